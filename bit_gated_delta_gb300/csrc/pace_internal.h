@@ -1,0 +1,52 @@
+// Internal declarations shared by the host runtime and the kernels of libpace.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pace.h"
+
+// Device view of one state, passed by value to every kernel (fits in the kernel parameter space).
+struct PaceDev {
+  int B, H, D, G, NG, dP;
+  int zero_point, buf_mode, state_mode, io;
+  int H4, H8;
+  uint32_t *codes4;        // [B][H4][D/8][D]
+  uint32_t *codes8;        // [B][H8][D/4][D]
+  __nv_bfloat16 *scale;    // [B][H][NG][D]
+  uint8_t *zp;             // [B][H][NG][D]
+  void *buf_k;             // int8 [B][H][dP][D] | packed int4 [B][H][dP][D/2] | f32 [B][H][dP][D]
+  void *buf_v;             // int8 [B][H][dP][D] | bf16 | f32
+  float *buf_s;            // [B][H][dP][4]: a, beta, s_k, s_v
+  int32_t *m;              // [B][H]
+  void *S;                 // f32 / bf16 [B][H][D][D]
+  uint8_t head_is_int8[PACE_MAX_HEADS];
+  int16_t head_slot[PACE_MAX_HEADS];
+};
+
+struct pace_state {
+  pace_config cfg;
+  int batch;
+  pace_layout lay;
+  char *base;
+  size_t bytes;
+  PaceDev dev;
+};
+
+// Per-call pointers of one decode step / flush / prefill chunk.
+struct PaceIO {
+  const void *q, *k, *v;
+  const float *a, *beta;
+  void *o;
+  int n;            // tokens (prefill) ; decode: 1 ; flush: 0
+};
+
+// Kernel launchers (each returns the launch status; nothing synchronises).
+cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
+cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
+cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
+cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s);
+cudaError_t pace_launch_dequantize_state(const PaceDev &d, float *S, cudaStream_t s);
+cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, float *e_out,
+                              cudaStream_t s);

@@ -1,0 +1,177 @@
+// State conversion hooks and the calibration statistic of the head ranking.
+//   quantize_state:   fp32 S [B,H,D,D] -> resident format (key-axis group quantizer, [P1] 무엇과 다른가)
+//   dequantize_state: resident format -> fp32 S
+//   calib:            e[b,h] = || Q(S) - S ||_F^2 of an fp32 state, the error energy of one rounding that
+//                     the ranking E_h = e_h / (1 - a_h^(2 dP)) uses ([P1] 무엇과 다른가).
+// One CTA per unit, one thread per column; groups are thread-local.
+#include "pace_common.cuh"
+
+namespace pace {
+
+template <int D, int G, int BITS>
+__device__ void quantize_column(const PaceDev &st, long unit, int b, int h, const float *Sg) {
+  constexpr int KPW = 32 / BITS, NWC = D / KPW, NG = D / G, WPG = G / KPW;
+  const int j = threadIdx.x;
+  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * NWC * D
+                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * NWC * D;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    float x[G];
+#pragma unroll
+    for (int ii = 0; ii < G; ++ii) x[ii] = Sg[(g * G + ii) * D + j];
+    uint32_t uq[G];
+    float s;
+    int z;
+    quant_group<G, BITS>(x, st.zero_point, uq, s, z);
+#pragma unroll
+    for (int ww = 0; ww < WPG; ++ww) {
+      uint32_t word = 0;
+      if (BITS == 4) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) word |= (uq[8 * ww + t] | (uq[8 * ww + 4 + t] << 4)) << (8 * t);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) word |= uq[4 * ww + t] << (8 * t);
+      }
+      codes[(g * WPG + ww) * D + j] = word;
+    }
+    st.scale[(unit * NG + g) * D + j] = __float2bfloat16_rn(s);
+    if (st.zero_point) st.zp[(unit * NG + g) * D + j] = (uint8_t)z;
+  }
+}
+
+template <int D, int G, int BITS>
+__device__ void dequantize_column(const PaceDev &st, long unit, int b, int h, float *So) {
+  constexpr int KPW = 32 / BITS, NWC = D / KPW, NG = D / G;
+  const int j = threadIdx.x;
+  const uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * NWC * D
+                                    : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * NWC * D;
+  for (int i = 0; i < D; ++i) {
+    const int g = i / G;
+    const float s = __bfloat162float(st.scale[(unit * NG + g) * D + j]);
+    const int z = st.zero_point ? (int)st.zp[(unit * NG + g) * D + j] : (1 << (BITS - 1));
+    const uint32_t w = codes[(i / KPW) * D + j];
+    const uint32_t u = BITS == 4 ? nibble_of(w, i % KPW) : byte_of(w, i % KPW);
+    So[i * D + j] = s * (float)((int)u - z);
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(D) quantize_state_kernel(const PaceDev st, const float *S) {
+  const long unit = blockIdx.x;
+  const int b = (int)(unit / st.H), h = (int)(unit - (long)b * st.H);
+  const int j = threadIdx.x;
+  const float *Sg = S + unit * D * D;
+  if (st.state_mode == PACE_STATE_QUANT) {
+    if (st.head_is_int8[h]) quantize_column<D, G, 8>(st, unit, b, h, Sg);
+    else quantize_column<D, G, 4>(st, unit, b, h, Sg);
+  } else if (st.state_mode == PACE_STATE_FP32) {
+    float *Sd = static_cast<float *>(st.S) + unit * D * D;
+    for (int i = 0; i < D; ++i) Sd[i * D + j] = Sg[i * D + j];
+  } else {
+    __nv_bfloat16 *Sd = static_cast<__nv_bfloat16 *>(st.S) + unit * D * D;
+    for (int i = 0; i < D; ++i) Sd[i * D + j] = __float2bfloat16_rn(Sg[i * D + j]);
+  }
+  if (j == 0) st.m[unit] = 0;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(D) dequantize_state_kernel(const PaceDev st, float *S) {
+  const long unit = blockIdx.x;
+  const int b = (int)(unit / st.H), h = (int)(unit - (long)b * st.H);
+  const int j = threadIdx.x;
+  float *So = S + unit * D * D;
+  if (st.state_mode == PACE_STATE_QUANT) {
+    if (st.head_is_int8[h]) dequantize_column<D, G, 8>(st, unit, b, h, So);
+    else dequantize_column<D, G, 4>(st, unit, b, h, So);
+  } else if (st.state_mode == PACE_STATE_FP32) {
+    const float *Ss = static_cast<const float *>(st.S) + unit * D * D;
+    for (int i = 0; i < D; ++i) So[i * D + j] = Ss[i * D + j];
+  } else {
+    const __nv_bfloat16 *Ss = static_cast<const __nv_bfloat16 *>(st.S) + unit * D * D;
+    for (int i = 0; i < D; ++i) So[i * D + j] = __bfloat162float(Ss[i * D + j]);
+  }
+}
+
+template <int D, int G, int BITS>
+__global__ void __launch_bounds__(D) calib_kernel(const PaceDev st, int zero_point, float *e_out) {
+  constexpr int NG = D / G;
+  __shared__ float red[32];
+  const long unit = blockIdx.x;
+  const int j = threadIdx.x;
+  const float *Sg = static_cast<const float *>(st.S) + unit * D * D;
+  float e = 0.0f;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    float x[G];
+#pragma unroll
+    for (int ii = 0; ii < G; ++ii) x[ii] = Sg[(g * G + ii) * D + j];
+    uint32_t uq[G];
+    float s;
+    int z;
+    quant_group<G, BITS>(x, zero_point, uq, s, z);
+#pragma unroll
+    for (int ii = 0; ii < G; ++ii) {
+      const float d = s * (float)((int)uq[ii] - z) - x[ii];
+      e = fmaf(d, d, e);
+    }
+  }
+  e = warp_sum(e);
+  if ((j & 31) == 0) red[j >> 5] = e;
+  __syncthreads();
+  if (j == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < D / 32; ++w) t += red[w];
+    e_out[unit] = t;
+  }
+}
+
+template <int D>
+static cudaError_t launch_calib_t(const PaceDev &d, int bits, int group, int zp, float *e, cudaStream_t s) {
+  const unsigned units = (unsigned)(d.B * d.H);
+  if (units == 0) return cudaSuccess;
+  if (group == 64) {
+    if (bits == 8) calib_kernel<D, 64, 8><<<units, D, 0, s>>>(d, zp, e);
+    else calib_kernel<D, 64, 4><<<units, D, 0, s>>>(d, zp, e);
+  } else {
+    if (bits == 8) calib_kernel<D, 32, 8><<<units, D, 0, s>>>(d, zp, e);
+    else calib_kernel<D, 32, 4><<<units, D, 0, s>>>(d, zp, e);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pace
+
+using namespace pace;
+
+cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s) {
+  const unsigned units = (unsigned)(d.B * d.H);
+  if (units == 0) return cudaSuccess;
+  if (d.D == 128) {
+    if (d.G == 64) quantize_state_kernel<128, 64><<<units, 128, 0, s>>>(d, S);
+    else quantize_state_kernel<128, 32><<<units, 128, 0, s>>>(d, S);
+  } else {
+    if (d.G == 64) quantize_state_kernel<64, 64><<<units, 64, 0, s>>>(d, S);
+    else quantize_state_kernel<64, 32><<<units, 64, 0, s>>>(d, S);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t pace_launch_dequantize_state(const PaceDev &d, float *S, cudaStream_t s) {
+  const unsigned units = (unsigned)(d.B * d.H);
+  if (units == 0) return cudaSuccess;
+  if (d.D == 128) {
+    if (d.G == 64) dequantize_state_kernel<128, 64><<<units, 128, 0, s>>>(d, S);
+    else dequantize_state_kernel<128, 32><<<units, 128, 0, s>>>(d, S);
+  } else {
+    if (d.G == 64) dequantize_state_kernel<64, 64><<<units, 64, 0, s>>>(d, S);
+    else dequantize_state_kernel<64, 32><<<units, 64, 0, s>>>(d, S);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, float *e_out,
+                              cudaStream_t s) {
+  return d.D == 128 ? launch_calib_t<128>(d, bits, group, zero_point, e_out, s)
+                    : launch_calib_t<64>(d, bits, group, zero_point, e_out, s);
+}

@@ -1,0 +1,168 @@
+/*
+ * pace.h -- C ABI of libpace, the GB300 (sm_103a) implementation of the PACE decode hot path.
+ *
+ * PACE stores the recurrent state of a gated-delta linear-attention layer -- one d_k x d_v matrix per
+ * (sequence, head) -- as int4 (int8 for a quarter of the heads in PACE-4/8) codes whose scales are
+ * shared by g contiguous elements along the key axis of one column. The state is rounded once every
+ * dP decoded tokens; the tokens in between wait in an int8 decode buffer and are replayed through the
+ * gated delta rule at every step. Prefill runs in 256-token chunks and rounds once per chunk.
+ *
+ * Pages (cited by title and section):
+ *   [P1] "PACE는 4비트 순환 상태를 주기적으로 반올림해 추론 메모리를 줄인다" (onedev.kr summary)
+ *   [P2] "[논문리뷰] PACE: Periodic and Channel-Aligned Encoding of Four-Bit Recurrent States"
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller unless stated otherwise; the library
+ *     never allocates device memory. `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Calls enqueue work on `stream` and return without synchronising. Argument errors are detected on
+ *     the host and returned before anything is launched; a failed launch returns PACE_ERR_CUDA.
+ *     pace_last_error() gives a message for the last failure of the calling thread.
+ *   - q, k [B, H, d_k], v and o [B, H, d_v] (decode) or [B, H, n, d] (prefill) are dense row-major
+ *     tensors of the configured I/O type (bf16 or fp32); a and beta are fp32 [B, H] or [B, H, n].
+ *   - The library does not L2-normalise k, does not scale q, and applies no output gate or norm.
+ *   - Calls on one state must not overlap on the GPU (same stream, or ordered by events).
+ */
+#ifndef PACE_H
+#define PACE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PACE_OK = 0,
+  PACE_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or config field */
+  PACE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  PACE_ERR_STATE = 3,        /* state handle cannot take this call (e.g. wrong mode) */
+  PACE_ERR_CUDA = 4,         /* a CUDA call failed; see pace_last_error() */
+  PACE_ERR_TIMEOUT = 5       /* reserved: a bounded device wait gave up */
+} pace_status;
+
+/* Resident state format. */
+enum {
+  PACE_STATE_QUANT = 0,      /* PACE: int4/int8 codes + bf16 key-axis group scales (+ zero points) */
+  PACE_STATE_FP32 = 1,       /* unquantized test mode: fp32 state, fp32 buffer, same periodic schedule */
+  PACE_STATE_BF16 = 2        /* comparison kernel: bf16 state read and written every token, no buffer */
+};
+/* Decode-buffer format ([P1] 어떻게 동작하나: int8 keys and values in the uniform configuration, 4-bit keys
+ * and bf16 values in the mixed configuration). */
+enum { PACE_BUF_INT8 = 0, PACE_BUF_MIXED = 1, PACE_BUF_FP32 = 2 };
+enum { PACE_IO_BF16 = 0, PACE_IO_F32 = 1 };
+
+#define PACE_MAX_HEADS 256
+#define PACE_MAX_DP 32
+
+/* Immutable configuration of one state ([P1] 무엇과 다른가, 어떻게 동작하나). */
+typedef struct {
+  int n_heads;        /* H, 1..PACE_MAX_HEADS */
+  int d_k, d_v;       /* head dims; this build: d_k == d_v, 64 or 128 */
+  int max_batch;      /* sequences the device memory is sized for */
+  int dP;             /* decode period, 1..PACE_MAX_DP (pages' default 8) */
+  int group;          /* key-axis group size g: 32 or 64, divides d_k (PACE-4: 64, PACE-4/8: 32) */
+  int zero_point;     /* 0: symmetric codes (PACE-4); 1: integer zero point (PACE-4/8) */
+  int buf_mode;       /* PACE_BUF_*; PACE_STATE_FP32 requires PACE_BUF_FP32 */
+  int state_mode;     /* PACE_STATE_* */
+  int prefill_chunk;  /* tokens rounded together in prefill; must be 256 ([P1] 어떻게 동작하나) */
+  int io_dtype;       /* PACE_IO_* for q, k, v, o */
+} pace_config;
+
+typedef struct pace_state pace_state;   /* opaque host handle */
+
+/* Byte offsets (from the state's device base) and strides of the resident arrays, for checkpoint
+ * tooling and tests. Unused arrays have offset (size_t)-1. Units are u = b*H + h.
+ *   codes4  uint32 [B][H4][d_k/8][d_v]  int4 heads: word (w, j) holds keys 8w..8w+7 of column j; byte t
+ *                                      has key 8w+t in its low nibble and key 8w+4+t in its high nibble
+ *   codes8  uint32 [B][H8][d_k/4][d_v]  int8 heads: byte t of word (w, j) holds key 4w+t of column j
+ *           stored codes are unsigned: symmetric code c is stored as c+8 (int4) / c+128 (int8);
+ *           zero-point codes are stored as they are
+ *   scale   bf16   [B][H][d_k/g][d_v]   group scales
+ *   zp      uint8  [B][H][d_k/g][d_v]   zero points (zero-point mode)
+ *   buf_k   int8   [B][H][dP][d_k]      int8 buffer; mixed: uint8 [B][H][dP][d_k/2], key 2t in the low
+ *                                      nibble of byte t, 2t+1 in the high one, stored as code+8;
+ *                                      fp32 buffer: float [B][H][dP][d_k]
+ *   buf_v   int8   [B][H][dP][d_v]      mixed: bf16 values; fp32 buffer: float
+ *   buf_s   float  [B][H][dP][4]        a_t, beta_t, key scale, value scale
+ *   m       int32  [B][H]               tokens in the buffer
+ *   S       float/bf16 [B][H][d_k][d_v] state of PACE_STATE_FP32 / PACE_STATE_BF16
+ * head_slot[h] is the index of head h inside its pool (codes4 or codes8). */
+typedef struct {
+  size_t codes4, codes8, scale, zp, buf_k, buf_v, buf_s, m, S;
+  size_t total_bytes;
+  int H4, H8;
+  int head_slot[PACE_MAX_HEADS];
+  uint8_t head_is_int8[PACE_MAX_HEADS];
+} pace_layout;
+
+/* Device bytes a state for cfg->max_batch sequences needs. head_is_int8 is NULL (all heads int4) or
+ * an H-byte host mask of heads kept at 8 bits (PACE-4/8, [P1] 무엇과 다른가). */
+pace_status pace_state_bytes(const pace_config *cfg, const uint8_t *head_is_int8, size_t *bytes_out);
+
+/* Bind a caller-owned device region of `bytes` (>= pace_state_bytes, 256-byte aligned) to a new state
+ * handle for `batch` (1..max_batch) sequences, and enqueue its zeroing on `stream` (zero state,
+ * empty buffers). The handle is host memory; release it with pace_state_free. */
+pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8, void *device_mem,
+                             size_t bytes, int batch, void *stream, pace_state **out);
+/* Frees the host handle only; the device region stays the caller's. NULL is accepted. */
+void pace_state_free(pace_state *state);
+pace_status pace_state_get_layout(const pace_state *state, pace_layout *out);
+
+/* One prefill chunk of n_tokens (0..256) for every sequence ([P1] 어떻게 동작하나: the chunk kernel writes
+ * the state once per chunk). Units with a pending decode buffer are flushed first. q, k [B,H,n,d_k],
+ * v, o [B,H,n,d_v], a, beta [B,H,n]. The state is rounded once at the end of the chunk. */
+pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, const void *k, const void *v,
+                               const float *a, const float *beta, void *o, void *stream);
+
+/* One decode token for every sequence ([P1] 어떻게 동작하나; [P2] 1. Key Terms & Definitions): append
+ * (k_t, v_t, a_t, beta_t) to the buffer, replay the buffered tokens from the rounded state through
+ * S_t = a_t S_{t-1} + k_t u_t^T, u_t = beta_t (v_t - (a_t S_{t-1})^T k_t), emit o_t = S_t^T q_t, and
+ * when the buffer holds dP tokens, round the state once and empty the buffer.
+ * q, k [B,H,d_k], v, o [B,H,d_v], a, beta [B,H]. In PACE_STATE_BF16 mode: no buffer, the bf16 state
+ * is read, updated and written every token (the pages' per-token comparison point, [P1] 전제와 한계). */
+pace_status pace_decode_step(pace_state *state, const void *q, const void *k, const void *v, const float *a,
+                             const float *beta, void *o, void *stream);
+
+/* Apply every pending buffer to its state, round once, and empty the buffers ([P1] 어떻게 동작하나:
+ * buffered tokens are applied to the state together at the flush). */
+pace_status pace_flush(pace_state *state, void *stream);
+
+/* Host-only head ranking ([P1] 무엇과 다른가; [P2] 3. Method & Key Results): E_h = e_h / (1 - a_h^(2 dP))
+ * (+inf for a_h >= 1); marks the floor(H*frac) heads with the largest E_h (ties: lower index).
+ * e_h, a_h, mask_out are HOST arrays of H entries. Deterministic, no GPU needed. */
+pace_status pace_assign_heads(const float *e_h, const float *a_h, int H, int dP, float frac,
+                              uint8_t *mask_out);
+
+/* Set the resident state from fp32 states S [B,H,d_k,d_v] (device): quantize with the configured
+ * key-axis quantizer (PACE_STATE_QUANT), copy (FP32) or round to bf16 (BF16); empties the buffers. */
+pace_status pace_quantize_state(pace_state *state, const float *S, void *stream);
+/* Write the resident state (without the pending buffer) as fp32 S_out [B,H,d_k,d_v] (device). */
+pace_status pace_dequantize_state(const pace_state *state, float *S_out, void *stream);
+
+/* Calibration for the head ranking: e_out[b*H+h] = || Q(S) - S ||_F^2 for the fp32 state of a
+ * PACE_STATE_FP32 handle, with the key-axis quantizer (bits, group, zero_point). e_out: device, fp32. */
+pace_status pace_calib_error_energy(const pace_state *fp32_state, int bits, int group, int zero_point,
+                                    float *e_out, void *stream);
+
+/* Checkpoint / resume: copy the whole resident region (codes, scales, zero points, buffers, m) to or
+ * from `bytes` bytes at dst/src, which may be host or device memory. Enqueued on `stream`. */
+pace_status pace_state_export(const pace_state *state, void *dst, size_t bytes, void *stream);
+pace_status pace_state_import(pace_state *state, const void *src, size_t bytes, void *stream);
+
+/* Resident bits per state value ([P1] 어떻게 동작하나, 무엇과 다른가). literal_formula != 0: payload
+ * b + (16 + zero-point bits)/g averaged over heads, plus the buffer cost c*dP with
+ * c = (b_k d_k + b_v d_v + 32)/(d_k d_v) (one value head per key head); literal_formula == 0: the bytes
+ * this library actually keeps per state value (codes, scales, zero points, buffer, counters) * 8.
+ * head_is_int8 as for pace_state_bytes. Returns a negative value for an invalid config. */
+double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, int literal_formula);
+
+/* Message for the last non-OK status returned to the calling thread ("" if none). */
+const char *pace_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int pace_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PACE_H */
