@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of the PACE decode step (one layer, all sequences of the batch, one token per step).
+
+Default workload: 32 heads, d_k = d_v = 128, batch 64, dP = 8, symmetric int4 state with key-axis groups
+of 64, int8 decode buffer, bf16 q/k/v/o, after a 512-token prefill in two 256-token chunks.
+
+Timing: CUDA events on the launching stream around exactly K decode steps (captured in CUDA graphs),
+after W warm-up steps, with a device synchronize on both sides. Step s uses state set s mod R: R
+independent state sets (one per "layer") rotate so that the working set is several times the 129 MB
+L2, and the sets are staggered by buffer phase, so every window of R steps holds each of the dP phases
+(append-only steps and the rounding step) equally often. `value` is sequences x steps / second.
+
+Extra objects on the JSON line: `roofline` (algorithmic bytes of the decode kernel per launch over its
+measured duration, against the measured HBM copy peak), `cpu_baseline` (the CPU oracle on a bounded
+sample, host cores), `e2e` (the same metric with host buffers: pinned host->device inputs and the
+device->host output copy inside the timed region), `bf16_pertoken` (the per-token bf16-state kernel,
+the pages' comparison point), `prefill`, and `clocks`.
+
+`--impl reference` times the CPU oracle (the reference arm of this build) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+ROTATE_TARGET = 4 * L2_BYTES
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=1000)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--batch", type=int, default=64)
+    p.add_argument("--extra", type=int, default=1, help="also time batch 128, the bf16 kernel and prefill")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    return p.parse_args(argv)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in getattr(self, "lines", []):
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def decode_bytes_per_unit(D: int, g: int, dP: int, m0: int, zp: int = 0, bits: int = 4, mixed: int = 0) -> int:
+    """Algorithmic bytes one decode step of one unit moves when the buffer holds m0 tokens before it:
+    packed codes and group scales (and zero points) read, the buffered entries read, the new entry
+    written, q/k/v/a/beta read and o written, the counter, and on the rounding step the state written."""
+    ng = D // g
+    state = D * D * bits // 8 + ng * D * 2 + (ng * D if zp else 0)
+    entry = (D // 2 + 2 * D + 16) if mixed else (2 * D + 16)
+    io = 3 * D * 2 + D * 2 + 8
+    b = state + m0 * entry + entry + io + 8
+    if m0 + 1 == dP:
+        b += state
+    return b
+
+
+def decode_bytes_period_avg(D, g, dP, **kw) -> float:
+    return sum(decode_bytes_per_unit(D, g, dP, m0, **kw) for m0 in range(dP)) / dP
+
+
+def bf16_bytes_per_unit(D: int) -> int:
+    return 2 * D * D * 2 + 3 * D * 2 + D * 2 + 8
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode.cu", "bit_gated_delta_gb300/csrc/pace_common.cuh",
+                  "bit_gated_delta_gb300/csrc/pace_internal.h"]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d[kernel][workload]
+        if rec.get("source_digest") == source_digest(DECODE_SOURCES):
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------------------------------------------
+# GPU arm
+
+class DecodeSetup:
+    """R state sets of one workload, prefilled and staggered by buffer phase, plus device-resident
+    decode inputs (NI distinct tokens)."""
+
+    NI = 8
+
+    def __init__(self, P, torch, wl, state_mode, R, prefill_tokens=512):
+        import synth
+        self.P, self.torch, self.wl = P, torch, wl
+        bf16 = state_mode == P.PACE_STATE_BF16
+        self.cfg = P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, zero_point=wl.zero_point,
+                                 buf_mode=P.PACE_BUF_MIXED if wl.mixed_buffer else P.PACE_BUF_INT8,
+                                 state_mode=state_mode)
+        self.states = [P.PaceState(self.cfg, wl.B) for _ in range(R)]
+        self.R = R
+        o = torch.empty(wl.B, wl.H, 256, wl.d_v, dtype=torch.bfloat16, device="cuda")
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.prefill_ms = 0.0
+        for c, t0 in enumerate(range(0, prefill_tokens, 256)):
+            x = synth.device_chunk_inputs(wl, t0, 256)
+            ev0.record()
+            self.states[0].prefill_chunk(x["q"], x["k"], x["v"], x["a"], x["beta"], o)
+            ev1.record()
+            torch.cuda.synchronize()
+            self.prefill_ms += ev0.elapsed_time(ev1)
+        self.prefill_tokens = prefill_tokens
+        src = self.states[0].region()
+        for st in self.states[1:]:
+            st.region().copy_(src)
+        x = synth.device_chunk_inputs(wl, prefill_tokens, self.NI)
+        self.inputs = [{k: (v[:, :, i].contiguous()) for k, v in x.items()} for i in range(self.NI)]
+        self.o = torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16, device="cuda")
+        if not bf16:
+            for r, st in enumerate(self.states):
+                for i in range(r % wl.dP):
+                    self.step_on(st, i)
+        torch.cuda.synchronize()
+
+    def step_on(self, st, i, stream=None):
+        x = self.inputs[i % self.NI]
+        st.decode_step(x["q"], x["k"], x["v"], x["a"], x["beta"], self.o, stream)
+
+    def graph(self, n_steps):
+        """A CUDA graph of n_steps consecutive decode steps over the rotating sets."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(2):                       # warm the launch path outside the capture
+                self.step_on(self.states[i % self.R], i)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                self.step_on(self.states[i % self.R], i)
+        return g
+
+    def close(self):
+        for st in self.states:
+            st.close()
+
+
+def time_steps(torch, setup, K, W, sampler=None):
+    """Run W warm-up steps, then exactly K timed steps; returns ms per step (CUDA events)."""
+    G = setup.R * setup.wl.dP if setup.cfg.state_mode != 2 else setup.R
+    G = min(G, max(1, K))
+    g = setup.graph(G)
+    for _ in range((W + G - 1) // G):
+        g.replay()
+    tail = K % G
+    gt = setup.graph(tail) if tail else None
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        torch.cuda.synchronize()
+        ev0.record()
+        for _ in range(K // G):
+            g.replay()
+        if gt is not None:
+            gt.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / K
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_e2e(torch, P, setup, K):
+    """Same metric through the public API with host buffers: per step, pinned host -> device copies of
+    q, k, v, a, beta, the decode call, and the device -> host copy of o, all inside the timed region."""
+    wl = setup.wl
+    host = []
+    for i in range(DecodeSetup.NI):
+        host.append({k: v.cpu().pin_memory() for k, v in setup.inputs[i].items()})
+    dev = {k: torch.empty_like(v) for k, v in setup.inputs[0].items()}
+    o_host = torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = o_host.numel() * o_host.element_size()
+    n = min(K, 2000)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(n):
+        x = host[i % DecodeSetup.NI]
+        for key in dev:
+            dev[key].copy_(x[key], non_blocking=True)
+        setup.states[i % setup.R].decode_step(dev["q"], dev["k"], dev["v"], dev["a"], dev["beta"], setup.o)
+        o_host.copy_(setup.o, non_blocking=True)
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / n
+    return {"value": wl.B / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": n}
+
+
+# ------------------------------------------------------------------------------------------------------
+# CPU oracle (the baseline, and the reference arm)
+
+def oracle_decode_rate(wl, budget_s: float, n_units: int = 32):
+    """Decode tokens/s of the CPU oracle on a bounded sample: n_units units of one sequence, prefilled
+    with 512 tokens, then whole decode periods until the time budget is used (OpenMP over units)."""
+    import oracle as O
+    import synth
+    wl1 = wl.with_(B=1, H=n_units)
+    cfg = O.Cfg(d_k=wl.d_k, d_v=wl.d_v, g=wl.g, bits=4, zero_point=wl.zero_point, dP=wl.dP,
+                buf_mode=O.BUF_MIXED if wl.mixed_buffer else O.BUF_INT8)
+    units = [O.Unit(cfg) for _ in range(n_units)]
+    for t0 in range(0, 512, 256):
+        x = synth.chunk_inputs(wl1, t0, 256)
+        for h, u in enumerate(units):
+            O.prefill(u, x["q"][0, h], x["k"][0, h], x["v"][0, h], x["a"][0, h], x["beta"][0, h])
+    toks = [synth.token_inputs(wl1, 512 + i) for i in range(wl.dP)]
+    threads = O.max_threads()
+    steps = 0
+    t_start = time.perf_counter()
+    while True:
+        for i in range(wl.dP):
+            x = toks[i]
+            O.decode_batch(units, x["q"][0], x["k"][0], x["v"][0], x["a"][0], x["beta"][0], nthreads=threads)
+        steps += wl.dP
+        el = time.perf_counter() - t_start
+        if el >= budget_s:
+            break
+    unit_steps_per_s = n_units * steps / el
+    tokens_per_s = unit_steps_per_s / wl.H          # one sequence token = H unit steps
+    return {"value": tokens_per_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_units} heads of one sequence, 512-token prefill, {steps} decode steps "
+                      f"({steps // wl.dP} periods), {el:.1f} s; tokens/s = unit-steps/s / {wl.H} heads"}
+
+
+def run_reference(args):
+    import synth
+    wl = synth.workload("pace4", B=args.batch)
+    budget = max(2.0, min(args.cpu_seconds, 60.0))
+    t0 = time.perf_counter()
+    cb = oracle_decode_rate(wl, budget)
+    wall = time.perf_counter() - t0
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.B / cb["value"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl, None),
+            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "PACE decode tokens/s (B=64-128, dP=8) and achieved HBM GB/s vs GB300 peak"
+
+
+def workload_config(wl, R):
+    c = {"workload": f"PACE-4 decode, 1 layer, H={wl.H}, d_k=d_v={wl.d_k}, batch {wl.B}, dP={wl.dP}, "
+                     f"key-axis g={wl.g} symmetric int4 state, int8 buffer, bf16 q/k/v/o, 512-token context",
+         "B": wl.B, "H": wl.H, "d": wl.d_k, "dP": wl.dP, "g": wl.g}
+    if R is not None:
+        c["l2"] = (f"inputs larger than L2: {R} independent state sets rotate (one per step), staggered by "
+                   f"buffer phase")
+    return c
+
+
+def rotation_count(nbytes: int, dP: int, align_dp: bool) -> int:
+    R = max(2, -(-ROTATE_TARGET // nbytes))
+    if align_dp:
+        R = -(-R // dP) * dP
+    return int(R)
+
+
+def measure(P, torch, wl, state_mode, K, W, sampler=None):
+    bytes1 = P.pace_state_bytes(P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, state_mode=state_mode,
+                                              buf_mode=P.PACE_BUF_INT8))
+    R = rotation_count(bytes1, wl.dP, state_mode == P.PACE_STATE_QUANT)
+    setup = DecodeSetup(P, torch, wl, state_mode, R)
+    ms = time_steps(torch, setup, K, W, sampler)
+    return setup, ms, R
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    import torch
+
+    import bit_gated_delta_gb300 as P
+    import synth
+    from bit_gated_delta_gb300 import build as B
+    if not B.up_to_date():
+        B.build()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    peak, peak_kind = read_peaks()
+    wl = synth.workload("pace4", B=args.batch)
+    K, W = max(1, args.steps), max(3, args.warmup)
+
+    sampler = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    setup, ms, R = measure(P, torch, wl, P.PACE_STATE_QUANT, K, W, sampler)
+    ms_t = torch.tensor([ms], device="cuda")
+    if dist:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = world * wl.B / (ms_max * 1e-3)
+    units = wl.B * wl.H
+    alg = units * decode_bytes_period_avg(wl.d_k, wl.g, wl.dP)
+    achieved = alg / (ms * 1e-3) / 1e9
+    traffic = recorded_traffic("decode_kernel", f"pace4_b{wl.B}")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_kernel<128,64>",
+                "algorithmic_bytes_per_launch": alg,
+                "note": "one decode_kernel launch per step; duration = event time of K graph-replayed steps / K"}
+    e2e = time_e2e(torch, P, setup, K)
+    e2e["value"] *= world
+    prefill = {"tokens": setup.prefill_tokens, "ms": setup.prefill_ms,
+               "tokens_per_s": wl.B * setup.prefill_tokens / (setup.prefill_ms * 1e-3)}
+    setup.close()
+    del setup
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if args.extra:
+        k2 = max(1000, K // 4)
+        for b in (64, 128):
+            wlb = synth.workload("pace4", B=b)
+            s2, ms2, R2 = measure(P, torch, wlb, P.PACE_STATE_BF16, k2, max(3, W // 4))
+            extra[f"bf16_pertoken_b{b}"] = {"tokens_per_s": b / (ms2 * 1e-3), "ms_per_step": ms2, "rotating_sets": R2,
+                                            "achieved_gbs": b * wlb.H * bf16_bytes_per_unit(128) / (ms2 * 1e-3) / 1e9}
+            s2.close()
+            if b == 128:
+                s3, ms3, R3 = measure(P, torch, wlb, P.PACE_STATE_QUANT, k2, max(3, W // 4))
+                alg3 = b * wlb.H * decode_bytes_period_avg(128, 64, 8)
+                extra["pace4_b128"] = {"tokens_per_s": b / (ms3 * 1e-3), "ms_per_step": ms3, "rotating_sets": R3,
+                                       "achieved_gbs": alg3 / (ms3 * 1e-3) / 1e9,
+                                       "frac": alg3 / (ms3 * 1e-3) / 1e9 / peak}
+                s3.close()
+            torch.cuda.empty_cache()
+
+    cb = None
+    if rank == 0 and world == 1:
+        cb = oracle_decode_rate(wl, args.cpu_seconds)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+                "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic", "config": workload_config(wl, R),
+                "roofline": roofline, "cpu_baseline": cb, "e2e": e2e, "gpu_launches": K,
+                "clocks": sampler.summary(), "prefill": prefill, **extra}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

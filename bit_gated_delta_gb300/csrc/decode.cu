@@ -461,6 +461,10 @@ __global__ void __launch_bounds__(D) decode_kernel(const PaceDev st, const PaceI
   const DecodeShared sh = decode_shared(smem, L);
 
   const int m0 = st.m[unit];
+  if (m0 < 0 || m0 >= st.dP) {                    // corrupted counter: leave the unit, emit zeros
+    if (has_token) store_io(io.o, unit * D + threadIdx.x, 0.0f, st.io);
+    return;
+  }
   if (!has_token && m0 == 0) return;              // flush with nothing pending
   const int mt = m0 + has_token;                  // tokens replayed
   const int do_flush = !has_token || mt == st.dP;
@@ -488,8 +492,13 @@ static cudaError_t launch_decode_t(const PaceDev &d, const PaceIO &io, int has_t
   const int fp32mode = d.state_mode == PACE_STATE_FP32;
   const size_t smem = decode_smem(D, d.dP, fp32mode).total;
   auto kern = decode_kernel<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  static size_t opted = 48 * 1024;                // dynamic shared memory allowed so far
+  if (smem > opted) {
+    const size_t most = decode_smem(D, PACE_MAX_DP, 1).total;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    if (e != cudaSuccess) return e;
+    opted = most;
+  }
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
   kern<<<units, D, smem, s>>>(d, io, has_token);

@@ -120,7 +120,9 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
  * S_t = a_t S_{t-1} + k_t u_t^T, u_t = beta_t (v_t - (a_t S_{t-1})^T k_t), emit o_t = S_t^T q_t, and
  * when the buffer holds dP tokens, round the state once and empty the buffer.
  * q, k [B,H,d_k], v, o [B,H,d_v], a, beta [B,H]. In PACE_STATE_BF16 mode: no buffer, the bf16 state
- * is read, updated and written every token (the pages' per-token comparison point, [P1] 전제와 한계). */
+ * is read, updated and written every token (the pages' per-token comparison point, [P1] 전제와 한계).
+ * A unit whose buffer counter is outside 0..dP-1 (e.g. after importing a corrupted region) is left
+ * unchanged and its output is zero. */
 pace_status pace_decode_step(pace_state *state, const void *q, const void *k, const void *v, const float *a,
                              const float *beta, void *o, void *stream);
 

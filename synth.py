@@ -111,8 +111,8 @@ def token_inputs(wl: Workload, t: int, layer: int = 0) -> dict:
     q = _rng(wl.seed, _T_Q, layer, t).standard_normal((B, H, wl.d_k))
     k = _rng(wl.seed, _T_K, layer, t).standard_normal((B, H, wl.d_k))
     v = _rng(wl.seed, _T_V, layer, t).standard_normal((B, H, wl.d_v))
-    q /= np.linalg.norm(q, axis=-1, keepdims=True)
-    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    q /= np.sqrt(np.einsum("...i,...i->...", q, q))[..., None]
+    k /= np.sqrt(np.einsum("...i,...i->...", k, k))[..., None]
     ch = outlier_channels(wl, layer)
     for h in range(H):
         v[:, h, ch[h]] *= wl.outlier_scale
@@ -129,5 +129,38 @@ def token_inputs(wl: Workload, t: int, layer: int = 0) -> dict:
 
 def chunk_inputs(wl: Workload, t0: int, n: int, layer: int = 0) -> dict:
     """Tokens t0 .. t0+n-1 stacked on axis 2: q, k [B, H, n, d_k], v [B, H, n, d_v], a, beta [B, H, n]."""
-    toks = [token_inputs(wl, t0 + i, layer) for i in range(n)]
-    return {key: np.stack([tk[key] for tk in toks], axis=2) for key in toks[0]}
+    out = None
+    for i in range(n):
+        tk = token_inputs(wl, t0 + i, layer)
+        if out is None:
+            out = {key: np.empty(val.shape[:2] + (n,) + val.shape[2:], np.float32) for key, val in tk.items()}
+        for key, val in tk.items():
+            out[key][:, :, i] = val
+    return out
+
+
+def device_chunk_inputs(wl: Workload, t0: int, n: int, layer: int = 0, device="cuda") -> dict:
+    """The same recipe drawn on the device with torch's Philox generator (seeded by workload seed, layer
+    and first token), for benchmarks that need many tokens quickly and no oracle comparison.
+    Returns torch tensors: q, k, v [B, H, n, d] in the I/O dtype, a, beta [B, H, n] fp32."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed((wl.seed * 1_000_003 + layer * 65_537 + t0) & 0x7FFFFFFFFFFFFFFF)
+    B, H = wl.B, wl.H
+    q = torch.randn(B, H, n, wl.d_k, generator=g, device=device)
+    k = torch.randn(B, H, n, wl.d_k, generator=g, device=device)
+    v = torch.randn(B, H, n, wl.d_v, generator=g, device=device)
+    q = q / q.norm(dim=-1, keepdim=True)
+    k = k / k.norm(dim=-1, keepdim=True)
+    ch = torch.from_numpy(outlier_channels(wl, layer)).to(device)
+    scale = torch.ones(H, wl.d_v, device=device)
+    scale.scatter_(1, ch, wl.outlier_scale)
+    v = v * scale[None, :, None, :]
+    if wl.a_per_head:
+        a = torch.from_numpy(head_decays(wl, layer)).to(device)[None, :, None].expand(B, H, n).contiguous()
+    else:
+        a = torch.rand(B, H, n, generator=g, device=device) * (wl.a_hi - wl.a_lo) + wl.a_lo
+    beta = torch.sigmoid(torch.randn(B, H, n, generator=g, device=device))
+    dt = torch.bfloat16 if wl.io == "bf16" else torch.float32
+    return {"q": q.to(dt).contiguous(), "k": k.to(dt).contiguous(), "v": v.to(dt).contiguous(),
+            "a": a.float().contiguous(), "beta": beta.float().contiguous()}

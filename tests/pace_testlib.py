@@ -1,0 +1,228 @@
+"""Helpers shared by the tests: building the library, decoding a state region, running the GPU path
+and the oracle side by side on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+import synth
+
+
+def ensure_built():
+    from bit_gated_delta_gb300 import build as B
+    B.build()
+    O.build()
+
+
+def bf16_bits_to_f32(u16: np.ndarray) -> np.ndarray:
+    return (u16.astype(np.uint32) << 16).view(np.float32)
+
+
+class Blob:
+    """Decoded view of a state region (bytes copied to the host), following the layout in pace.h."""
+
+    def __init__(self, raw: np.ndarray, layout, cfg, batch: int):
+        self.raw = raw
+        self.L = layout
+        self.cfg = cfg
+        self.B = batch
+        self.H = cfg.n_heads
+        self.D = cfg.d_k
+        self.NG = self.D // cfg.group
+
+    def _arr(self, off, dtype, shape):
+        n = int(np.prod(shape))
+        return np.frombuffer(self.raw, dtype=dtype, count=n, offset=off).reshape(shape)
+
+    def m(self):
+        return self._arr(self.L.m, np.int32, (self.B, self.H))
+
+    def scales(self):
+        return bf16_bits_to_f32(self._arr(self.L.scale, np.uint16, (self.B, self.H, self.NG, self.D)))
+
+    def zps(self):
+        return self._arr(self.L.zp, np.uint8, (self.B, self.H, self.NG, self.D)).astype(np.int32)
+
+    def codes(self, b: int, h: int) -> np.ndarray:
+        """Canonical codes [d_k][d_v] of unit (b, h), as the oracle writes them."""
+        D = self.D
+        is8 = bool(self.L.head_is_int8[h])
+        slot = self.L.head_slot[h]
+        if not is8:
+            w = self._arr(self.L.codes4, np.uint32, (self.B, self.L.H4, D // 8, D))[b, slot]
+            out = np.zeros((D, D), np.int32)
+            for t in range(4):
+                out[np.arange(D // 8) * 8 + t] = (w >> (8 * t)) & 0xF
+                out[np.arange(D // 8) * 8 + 4 + t] = (w >> (8 * t + 4)) & 0xF
+            off = 8
+        else:
+            w = self._arr(self.L.codes8, np.uint32, (self.B, self.L.H8, D // 4, D))[b, slot]
+            out = np.zeros((D, D), np.int32)
+            for t in range(4):
+                out[np.arange(D // 4) * 4 + t] = (w >> (8 * t)) & 0xFF
+            off = 128
+        return out if self.cfg.zero_point else out - off
+
+    def buffer(self, b: int, h: int):
+        """(key codes [dP, D], value codes or values [dP, D], scalars [dP, 4]) of unit (b, h)."""
+        D, P = self.D, self.cfg.dP
+        s = self._arr(self.L.buf_s, np.float32, (self.B, self.H, P, 4))[b, h]
+        if self.cfg.buf_mode == 1:
+            kb = self._arr(self.L.buf_k, np.uint8, (self.B, self.H, P, D // 2))[b, h]
+            k = np.zeros((P, D), np.int32)
+            k[:, 0::2] = (kb & 0xF).astype(np.int32) - 8
+            k[:, 1::2] = (kb >> 4).astype(np.int32) - 8
+            v = bf16_bits_to_f32(self._arr(self.L.buf_v, np.uint16, (self.B, self.H, P, D))[b, h])
+        elif self.cfg.buf_mode == 2:
+            k = self._arr(self.L.buf_k, np.float32, (self.B, self.H, P, D))[b, h]
+            v = self._arr(self.L.buf_v, np.float32, (self.B, self.H, P, D))[b, h]
+        else:
+            k = self._arr(self.L.buf_k, np.int8, (self.B, self.H, P, D))[b, h].astype(np.int32)
+            v = self._arr(self.L.buf_v, np.int8, (self.B, self.H, P, D))[b, h].astype(np.int32)
+        return k, v, s
+
+
+def read_blob(state) -> Blob:
+    import torch
+    torch.cuda.synchronize()
+    raw = state.region().cpu().numpy().tobytes()
+    return Blob(np.frombuffer(raw, np.uint8), state.layout, state.cfg, state.batch)
+
+
+def oracle_cfg(wl: synth.Workload, bits: int = 4, state_mode: int = O.STATE_QUANT) -> O.Cfg:
+    if state_mode == O.STATE_QUANT:
+        buf = O.BUF_MIXED if wl.mixed_buffer else O.BUF_INT8
+    else:
+        buf = O.BUF_FP32
+    return O.Cfg(d_k=wl.d_k, d_v=wl.d_v, g=wl.g, bits=bits, zero_point=wl.zero_point, dP=wl.dP, buf_mode=buf,
+                 state_mode=state_mode)
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
+
+
+def code_agreement(gpu_codes: np.ndarray, ref_codes: np.ndarray):
+    """(fraction identical, max |difference|)."""
+    d = np.abs(gpu_codes.astype(np.int64) - ref_codes.astype(np.int64))
+    return float((d == 0).mean()), int(d.max())
+
+
+class PairRun:
+    """Runs the CUDA path (through the C ABI) and the oracle on the same seeded workload inputs.
+
+    The GPU processes every unit; the oracle the units listed in `sample` ((b, h) pairs, default all).
+    Outputs are compared in the I/O precision: with bf16 I/O the oracle's output is rounded to bf16
+    (the same rounding decision the kernel takes), so the comparison measures the path, not the format.
+    """
+
+    def __init__(self, wl: synth.Workload, state_mode: int = 0, mask=None, sample=None, dP=None, layer=0):
+        import torch
+        import bit_gated_delta_gb300 as P
+        self.P, self.torch = P, torch
+        if dP is not None:
+            wl = wl.with_(dP=dP)
+        self.wl = wl
+        self.layer = layer
+        self.mask = np.zeros(wl.H, np.uint8) if mask is None else np.asarray(mask, np.uint8)
+        if state_mode == P.PACE_STATE_QUANT:
+            buf = P.PACE_BUF_MIXED if wl.mixed_buffer else P.PACE_BUF_INT8
+        elif state_mode == P.PACE_STATE_FP32:
+            buf = P.PACE_BUF_FP32
+        else:
+            buf = P.PACE_BUF_INT8
+        self.io_bf16 = wl.io == "bf16"
+        self.cfg = P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, zero_point=wl.zero_point, buf_mode=buf,
+                                 state_mode=state_mode,
+                                 io_dtype=P.PACE_IO_BF16 if self.io_bf16 else P.PACE_IO_F32)
+        self.state = P.PaceState(self.cfg, wl.B, self.mask if state_mode == 0 else None)
+        self.sample = sample if sample is not None else [(b, h) for b in range(wl.B) for h in range(wl.H)]
+        om = {0: O.STATE_QUANT, 1: O.STATE_FP32, 2: O.STATE_BF16}[state_mode]
+        self.units = {}
+        for (b, h) in self.sample:
+            c = oracle_cfg(wl, bits=8 if self.mask[h] else 4, state_mode=om)
+            if om == O.STATE_BF16:
+                c.buf_mode = O.BUF_FP32
+            self.units[(b, h)] = O.Unit(c)
+        self.t = 0
+
+    def _dev(self, x: np.ndarray, io: bool):
+        t = self.torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        return t.to(self.torch.bfloat16) if (io and self.io_bf16) else t
+
+    def _ref_out(self, ref: np.ndarray) -> np.ndarray:
+        if self.io_bf16:
+            return O.bf16_rn(ref.astype(np.float32)).astype(np.float64)
+        return ref
+
+    def prefill(self, n: int, inputs=None):
+        wl = self.wl
+        x = inputs if inputs is not None else synth.chunk_inputs(wl, self.t, n, self.layer)
+        o = self.torch.empty(wl.B, wl.H, n, wl.d_v, device="cuda",
+                             dtype=self.torch.bfloat16 if self.io_bf16 else self.torch.float32)
+        self.state.prefill_chunk(self._dev(x["q"], True), self._dev(x["k"], True), self._dev(x["v"], True),
+                                 self._dev(x["a"], False), self._dev(x["beta"], False), o)
+        got = o.float().cpu().numpy()
+        refs, gots = [], []
+        for (b, h), u in self.units.items():
+            r = O.prefill(u, x["q"][b, h], x["k"][b, h], x["v"][b, h], x["a"][b, h], x["beta"][b, h])
+            refs.append(self._ref_out(r))
+            gots.append(got[b, h])
+        self.t += n
+        self.last = got
+        return (np.stack(gots), np.stack(refs)) if refs else (got, None)
+
+    def decode(self, inputs=None):
+        wl = self.wl
+        x = inputs if inputs is not None else synth.token_inputs(wl, self.t, self.layer)
+        o = self.torch.empty(wl.B, wl.H, wl.d_v, device="cuda",
+                             dtype=self.torch.bfloat16 if self.io_bf16 else self.torch.float32)
+        self.state.decode_step(self._dev(x["q"], True), self._dev(x["k"], True), self._dev(x["v"], True),
+                               self._dev(x["a"], False), self._dev(x["beta"], False), o)
+        got = o.float().cpu().numpy()
+        refs, gots = [], []
+        for (b, h), u in self.units.items():
+            r = O.decode_step(u, x["q"][b, h], x["k"][b, h], x["v"][b, h], x["a"][b, h], x["beta"][b, h])
+            refs.append(self._ref_out(r))
+            gots.append(got[b, h])
+        self.t += 1
+        self.last = got
+        return (np.stack(gots), np.stack(refs)) if refs else (got, None)
+
+    def flush(self):
+        self.state.flush()
+        for u in self.units.values():
+            O.flush(u)
+
+    def blob(self) -> Blob:
+        return read_blob(self.state)
+
+    def codes_vs_oracle(self):
+        """(fraction of identical codes, max |difference|) over the sampled units."""
+        blob = self.blob()
+        g, r = [], []
+        for (b, h), u in self.units.items():
+            g.append(blob.codes(b, h))
+            r.append(u.code)
+        return code_agreement(np.stack(g), np.stack(r))
+
+    def state_vs_oracle(self) -> float:
+        """Relative L2 distance of the resident states (fp32 / bf16 modes)."""
+        out = self.torch.empty(self.wl.B, self.wl.H, self.wl.d_k, self.wl.d_v, device="cuda")
+        self.P.pace_dequantize_state(self.state.handle, out)
+        S = out.cpu().numpy()
+        return rel_l2(np.stack([S[b, h] for (b, h) in self.units]), np.stack([u.S for u in self.units.values()]))
+
+    def sync_oracle_from_gpu(self):
+        """Teacher forcing: copy the GPU's resident quantized state into the oracle units."""
+        blob = self.blob()
+        sc = blob.scales()
+        zps = blob.zps() if self.wl.zero_point else None
+        for (b, h), u in self.units.items():
+            u.code[...] = blob.codes(b, h)
+            u.scale[...] = sc[b, h]
+            if zps is not None:
+                u.zp[...] = zps[b, h]

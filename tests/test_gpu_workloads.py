@@ -1,0 +1,103 @@
+"""The synthetic workloads at their stated sizes (GPU): every unit runs on the GPU, the oracle follows a
+fixed sample of units, and properties that hold at any size are checked on all units."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from pace_testlib import PairRun, ensure_built, read_blob, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE64 = [(0, 0), (0, 31), (17, 5), (63, 31), (31, 16), (5, 7), (40, 20), (63, 0)]
+SAMPLE128 = [(0, 0), (127, 31), (64, 3), (100, 8), (9, 30), (77, 12)]
+
+
+@pytest.fixture(scope="module")
+def P():
+    ensure_built()
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import bit_gated_delta_gb300 as P
+    return P
+
+
+def test_pace4_batch64_full_schedule(P):
+    """32 heads, d=128, batch 64: 512-token prefill in two chunks, 256 decode tokens (32 roundings)."""
+    wl = synth.workload("pace4")
+    run = PairRun(wl, sample=SAMPLE64)
+    for _ in range(wl.prefill // 256):
+        g, r = run.prefill(256)
+        assert rel_l2(g, r) <= 1e-3
+    worst = 0.0
+    for step in range(wl.decode):
+        g, r = run.decode()
+        worst = max(worst, rel_l2(g, r))
+        assert np.isfinite(run.last).all()
+        if (step + 1) % wl.dP == 0:
+            frac, dmax = run.codes_vs_oracle()
+            assert frac >= 0.999 and dmax <= 1, (step, frac, dmax)
+    assert worst <= 1e-3, worst
+    assert (read_blob(run.state).m() == 0).all()
+
+
+def test_pace48_calibration_ranking_and_mixed_decode(P):
+    """PACE-4/8 at batch 128: calibrate e_h on an fp32 prefill, rank heads by E_h, run the mixed path."""
+    import torch
+    wl = synth.workload("pace48")
+    a_h = synth.head_decays(wl)
+    pre = [synth.chunk_inputs(wl, t0, 256) for t0 in range(0, wl.prefill, 256)]
+    # GPU calibration over all 128 sequences
+    cal = PairRun(wl, state_mode=P.PACE_STATE_FP32, sample=[(0, h) for h in range(wl.H)])
+    cal.wl = wl.with_(io="bf16")
+    for x in pre:
+        cal.prefill(256, inputs=x)
+    e = torch.zeros(wl.B * wl.H, device="cuda")
+    P.pace_calib_error_energy(cal.state.handle, 4, wl.g, 1, e)
+    e_unit = e.cpu().numpy().reshape(wl.B, wl.H)
+    # oracle error energy for sequence 0 from its own fp32 (fp64) prefill
+    ocfg = O.Cfg(d_k=128, d_v=128, g=wl.g, bits=4, zero_point=1)
+    e_ref = np.array([O.error_energy(ocfg, cal.units[(0, h)].S.astype(np.float32)) for h in range(wl.H)])
+    np.testing.assert_allclose(e_unit[0], e_ref, rtol=2e-2)
+    e_h = e_unit.mean(axis=0)
+    mask = P.pace_assign_heads(e_h, a_h, wl.dP, 0.25)
+    assert mask.sum() == 8
+    assert np.array_equal(mask, O.assign_heads(e_h.astype(np.float64), a_h.astype(np.float64), wl.dP, 0.25))
+    # the mixed path with that mask
+    run = PairRun(wl, mask=mask, sample=SAMPLE128 + [(3, int(np.flatnonzero(mask)[0]))])
+    for x in pre:
+        g, r = run.prefill(256, inputs=x)
+        assert rel_l2(g, r) <= 1e-3
+    for step in range(wl.decode):
+        g, r = run.decode()
+        assert rel_l2(g, r) <= 1e-3, step
+        if (step + 1) % wl.dP == 0 and step % 64 == 63:
+            frac, dmax = run.codes_vs_oracle()
+            assert frac >= 0.999 and dmax <= 1, (step, frac, dmax)
+
+
+@pytest.mark.parametrize("dP", [1, 8, 32])
+def test_longctx_shape_periods(P, dP):
+    """48 heads, batch 16, slow decay; a 1024-token prefill (4 chunks) then 64 decode tokens."""
+    wl = synth.workload("longctx")
+    run = PairRun(wl, dP=dP, sample=[(0, 0), (15, 47), (7, 20)])
+    for _ in range(4):
+        g, r = run.prefill(256)
+        assert rel_l2(g, r) <= 1e-3
+    for step in range(64):
+        g, r = run.decode()
+        assert rel_l2(g, r) <= 1e-3, (dP, step)
+    frac, dmax = run.codes_vs_oracle()
+    assert frac >= 0.999 and dmax <= 1
+
+
+def test_layer_stack_inputs(P):
+    """The batch-sweep shape (16 heads, d=128) on two independent layers at batch 2."""
+    wl = synth.workload("sweep", B=2)
+    for layer in (0, 23):
+        run = PairRun(wl, layer=layer)
+        g, r = run.prefill(256)
+        assert rel_l2(g, r) <= 1e-3
+        for _ in range(2 * wl.dP):
+            g, r = run.decode()
+            assert rel_l2(g, r) <= 1e-3
