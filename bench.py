@@ -435,7 +435,7 @@ def main():
             torch.cuda.empty_cache()
 
     cb = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         cb = oracle_decode_rate(wl, args.cpu_seconds)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,

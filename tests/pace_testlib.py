@@ -216,6 +216,14 @@ class PairRun:
         S = out.cpu().numpy()
         return rel_l2(np.stack([S[b, h] for (b, h) in self.units]), np.stack([u.S for u in self.units.values()]))
 
+    def check_round_and_sync(self):
+        """At a rounding: compare the GPU's codes with the oracle's (both rounded from the same starting
+        state of this period), then hand the GPU's rounded state to the oracle for the next period.
+        Returns (fraction identical, max |difference|)."""
+        res = self.codes_vs_oracle()
+        self.sync_oracle_from_gpu()
+        return res
+
     def sync_oracle_from_gpu(self):
         """Teacher forcing: copy the GPU's resident quantized state into the oracle units."""
         blob = self.blob()

@@ -25,7 +25,8 @@ def P():
 
 
 def check_codes(run, where):
-    frac, dmax = run.codes_vs_oracle()
+    """Codes of one rounding against the oracle's from the same starting state, then re-synchronise."""
+    frac, dmax = run.check_round_and_sync()
     assert frac >= CODE_FRAC and dmax <= 1, f"{where}: {frac:.5f} identical, max diff {dmax}"
     return frac
 
