@@ -25,7 +25,7 @@ def P():
 def test_pace4_batch64_full_schedule(P):
     """32 heads, d=128, batch 64: 512-token prefill in two chunks, 256 decode tokens (32 roundings)."""
     wl = synth.workload("pace4")
-    run = PairRun(wl, sample=SAMPLE64)
+    run = PairRun(wl, sample=SAMPLE64, out_f32=True)
     for _ in range(wl.prefill // 256):
         g, r = run.prefill(256)
         assert rel_l2(g, r) <= 1e-3
@@ -65,7 +65,6 @@ def test_pace48_calibration_ranking_and_mixed_decode(P):
     pre = [synth.chunk_inputs(wl, t0, 256) for t0 in range(0, wl.prefill, 256)]
     # GPU calibration over all 128 sequences
     cal = PairRun(wl, state_mode=P.PACE_STATE_FP32, sample=[(0, h) for h in range(wl.H)])
-    cal.wl = wl.with_(io="bf16")
     for x in pre:
         cal.prefill(256, inputs=x)
     e = torch.zeros(wl.B * wl.H, device="cuda")
@@ -80,7 +79,7 @@ def test_pace48_calibration_ranking_and_mixed_decode(P):
     assert mask.sum() == 8
     assert np.array_equal(mask, O.assign_heads(e_h.astype(np.float64), a_h.astype(np.float64), wl.dP, 0.25))
     # the mixed path with that mask
-    run = PairRun(wl, mask=mask, sample=SAMPLE128 + [(3, int(np.flatnonzero(mask)[0]))])
+    run = PairRun(wl, mask=mask, sample=SAMPLE128 + [(3, int(np.flatnonzero(mask)[0]))], out_f32=True)
     for x in pre:
         g, r = run.prefill(256, inputs=x)
         assert rel_l2(g, r) <= 1e-3
@@ -98,7 +97,7 @@ def test_pace48_calibration_ranking_and_mixed_decode(P):
 def test_longctx_shape_periods(P, dP):
     """48 heads, batch 16, slow decay; a 1024-token prefill (4 chunks) then 64 decode tokens."""
     wl = synth.workload("longctx")
-    run = PairRun(wl, dP=dP, sample=[(0, 0), (15, 47), (7, 20)])
+    run = PairRun(wl, dP=dP, sample=[(0, 0), (15, 47), (7, 20)], out_f32=True)
     for _ in range(4):
         g, r = run.prefill(256)
         assert rel_l2(g, r) <= 1e-3
@@ -116,7 +115,7 @@ def test_layer_stack_inputs(P):
     """The batch-sweep shape (16 heads, d=128) on two independent layers at batch 2."""
     wl = synth.workload("sweep", B=2)
     for layer in (0, 23):
-        run = PairRun(wl, layer=layer)
+        run = PairRun(wl, layer=layer, out_f32=True)
         g, r = run.prefill(256)
         assert rel_l2(g, r) <= 1e-3
         run.check_round_and_sync()
