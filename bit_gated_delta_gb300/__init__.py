@@ -18,7 +18,7 @@ __all__ = [
     "pace_config", "make_config", "pace_state_bytes", "pace_state_alloc", "pace_state_free",
     "pace_state_get_layout", "pace_prefill_chunk", "pace_decode_step", "pace_flush", "pace_assign_heads",
     "pace_quantize_state", "pace_dequantize_state", "pace_calib_error_energy", "pace_state_export",
-    "pace_state_import", "pace_resident_bits", "pace_last_error", "pace_version", "PaceState", "PaceError",
+    "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_last_error", "pace_version", "PaceState", "PaceError",
     "PACE_STATE_QUANT", "PACE_STATE_FP32", "PACE_STATE_BF16", "PACE_BUF_INT8", "PACE_BUF_MIXED",
     "PACE_BUF_FP32", "PACE_IO_BF16", "PACE_IO_F32", "PACE_MAX_HEADS", "PACE_MAX_DP",
 ]
@@ -128,6 +128,13 @@ def pace_state_export(handle, dst, nbytes: int, stream=None) -> None:
 
 def pace_state_import(handle, src, nbytes: int, stream=None) -> None:
     check(lib().pace_state_import(handle, _ptr(src), nbytes, _stream(stream)))
+
+
+def pace_get_status(handle, clear: bool = False, stream=None) -> int:
+    """Reads the state's device status word (synchronises the stream); raises PaceError on a timeout bit."""
+    out = C.c_int()
+    check(lib().pace_get_status(handle, int(clear), C.byref(out), _stream(stream)))
+    return out.value
 
 
 def pace_resident_bits(cfg: pace_config, head_is_int8=None, literal_formula: bool = True) -> float:

@@ -29,7 +29,7 @@ class pace_config(C.Structure):
 class pace_layout(C.Structure):
     _fields_ = [("codes4", C.c_size_t), ("codes8", C.c_size_t), ("scale", C.c_size_t), ("zp", C.c_size_t),
                 ("buf_k", C.c_size_t), ("buf_v", C.c_size_t), ("buf_s", C.c_size_t), ("m", C.c_size_t),
-                ("S", C.c_size_t), ("total_bytes", C.c_size_t), ("H4", C.c_int), ("H8", C.c_int),
+                ("S", C.c_size_t), ("status", C.c_size_t), ("total_bytes", C.c_size_t), ("H4", C.c_int), ("H8", C.c_int),
                 ("head_slot", C.c_int * PACE_MAX_HEADS), ("head_is_int8", C.c_uint8 * PACE_MAX_HEADS)]
 
 
@@ -61,6 +61,7 @@ _SIGS = {
     "pace_state_export": (_I, [_VP, _VP, _SZ, _VP]),
     "pace_state_import": (_I, [_VP, _VP, _SZ, _VP]),
     "pace_resident_bits": (_D, [C.POINTER(pace_config), _PU8, _I]),
+    "pace_get_status": (_I, [_VP, _I, C.POINTER(C.c_int), _VP]),
 }
 
 

@@ -77,7 +77,7 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
   pace_layout L;
   memset(&L, 0, sizeof L);
   const size_t none = (size_t)-1;
-  L.codes4 = L.codes8 = L.scale = L.zp = L.buf_k = L.buf_v = L.buf_s = L.m = L.S = none;
+  L.codes4 = L.codes8 = L.scale = L.zp = L.buf_k = L.buf_v = L.buf_s = L.m = L.S = L.status = none;
   const size_t B = (size_t)batch, H = (size_t)c->n_heads, D = (size_t)c->d_k, NG = D / (size_t)c->group;
   const size_t P = (size_t)c->dP;
   int h4 = 0, h8 = 0;
@@ -115,6 +115,7 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
     take(L.S, B * H * D * D * 2);
   }
   take(L.m, B * H * 4);
+  take(L.status, 4);
   L.total_bytes = off;
   return L;
 }
@@ -191,6 +192,7 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
   d.buf_v = at<void>(s->base, L.buf_v);
   d.buf_s = at<float>(s->base, L.buf_s);
   d.m = at<int32_t>(s->base, L.m);
+  d.status = at<int32_t>(s->base, L.status);
   d.S = at<void>(s->base, L.S);
   for (int h = 0; h < cfg->n_heads; ++h) {
     d.head_is_int8[h] = L.head_is_int8[h];
@@ -230,8 +232,13 @@ pace_status pace_decode_step(pace_state *state, const void *q, const void *k, co
     return fail(PACE_ERR_INVALID_ARG, "decode_step: a tensor pointer is NULL");
   PaceIO io{q, k, v, a, beta, o, 1};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = state->cfg.state_mode == PACE_STATE_BF16 ? pace_launch_decode_bf16(state->dev, io, cs)
-                                                           : pace_launch_decode(state->dev, io, 1, cs);
+  cudaError_t e;
+  if (state->cfg.state_mode == PACE_STATE_BF16)
+    e = pace_launch_decode_bf16(state->dev, io, cs);
+  else if (state->cfg.state_mode == PACE_STATE_QUANT)
+    e = pace_launch_decode_tc(state->dev, io, 1, cs);
+  else
+    e = pace_launch_decode(state->dev, io, 1, cs);
   if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
   return ok();
 }
@@ -241,7 +248,9 @@ pace_status pace_flush(pace_state *state, void *stream) {
   if (st != PACE_OK) return st;
   if (state->cfg.state_mode == PACE_STATE_BF16) return ok();   // no buffer
   PaceIO io{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-  cudaError_t e = pace_launch_decode(state->dev, io, 0, static_cast<cudaStream_t>(stream));
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_tc(state->dev, io, 0, cs)
+                                                            : pace_launch_decode(state->dev, io, 0, cs);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   return ok();
 }
@@ -259,7 +268,8 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
   cudaError_t e = cudaSuccess;
   if (state->cfg.state_mode != PACE_STATE_BF16) {
     PaceIO fio{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-    e = pace_launch_decode(state->dev, fio, 0, cs);            // pending buffers first
+    e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_tc(state->dev, fio, 0, cs)
+                                                  : pace_launch_decode(state->dev, fio, 0, cs);   // pending buffers first
     if (e != cudaSuccess) return cuda_fail(e, "prefill flush launch");
   }
   PaceIO io{q, k, v, a, beta, o, n_tokens};
@@ -322,6 +332,21 @@ pace_status pace_state_import(pace_state *state, const void *src, size_t bytes, 
     return fail(PACE_ERR_INVALID_ARG, "import expects exactly %zu bytes, got %zu", state->lay.total_bytes, bytes);
   cudaError_t e = cudaMemcpyAsync(state->base, src, bytes, cudaMemcpyDefault, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "state import copy");
+  return ok();
+}
+
+pace_status pace_get_status(const pace_state *state, int clear, int *status_out, void *stream) {
+  pace_status st = check_state(state);
+  if (st != PACE_OK) return st;
+  if (!status_out) return fail(PACE_ERR_INVALID_ARG, "status_out is NULL");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, state->dev.status, 4, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess && clear && word) e = cudaMemsetAsync(state->dev.status, 0, 4, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  *status_out = word;
+  if (word & 1) return fail(PACE_ERR_TIMEOUT, "a bounded device wait gave up");
   return ok();
 }
 

@@ -10,6 +10,13 @@
 
 namespace pace {
 
+// Sequential carving of a dynamic shared-memory block (16-byte aligned pieces, or `align`).
+__host__ __device__ inline size_t carve(size_t &off, size_t bytes, size_t align = 16) {
+  const size_t o = (off + align - 1) & ~(align - 1);
+  off = o + bytes;
+  return o;
+}
+
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 __device__ __forceinline__ float load_io(const void *p, long idx, int io) {
@@ -132,11 +139,22 @@ __device__ __forceinline__ float buffer_scale(float A, int qmax) {
   return __fdiv_rn(A, (float)qmax);
 }
 
-// Stored-code extraction from packed words (layouts in pace.h).
+// Stored-code extraction from packed words (layouts in pace.h). An int4 word holds keys 8w..8w+7 of one
+// column: key 8w+2s in bits 4s..4s+3 and key 8w+2s+1 in bits 16+4s..16+4s+3, so that masking the word
+// shifted by 4s with 0x000F000F yields the pair (key 2s, key 2s+1) in the two 16-bit halves.
+__device__ __forceinline__ int nibble_shift(int key_in_word) { return ((key_in_word & 1) << 4) | ((key_in_word >> 1) << 2); }
 __device__ __forceinline__ uint32_t nibble_of(uint32_t word, int key_in_word) {
-  // keys 0..3 of the word sit in the low nibbles of bytes 0..3, keys 4..7 in the high nibbles
-  const int sh = ((key_in_word & 3) << 3) + ((key_in_word >> 2) << 2);
-  return (word >> sh) & 0xFu;
+  return (word >> nibble_shift(key_in_word)) & 0xFu;
+}
+// Pack 8 stored int4 codes (keys 0..7 of a word) / 4 stored int8 codes.
+__device__ __forceinline__ uint32_t pack_nibbles(const uint32_t *u) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) w |= u[e] << nibble_shift(e);
+  return w;
+}
+__device__ __forceinline__ uint32_t pack_bytes(const uint32_t *u) {
+  return u[0] | (u[1] << 8) | (u[2] << 16) | (u[3] << 24);
 }
 __device__ __forceinline__ uint32_t byte_of(uint32_t word, int key_in_word) {
   return (word >> (key_in_word << 3)) & 0xFFu;

@@ -20,6 +20,7 @@ struct PaceDev {
   void *buf_v;             // int8 [B][H][dP][D] | bf16 | f32
   float *buf_s;            // [B][H][dP][4]: a, beta, s_k, s_v
   int32_t *m;              // [B][H]
+  int32_t *status;         // one word: bit 0 set when a bounded device wait gave up
   void *S;                 // f32 / bf16 [B][H][D][D]
   uint8_t head_is_int8[PACE_MAX_HEADS];
   int16_t head_slot[PACE_MAX_HEADS];
@@ -44,6 +45,7 @@ struct PaceIO {
 
 // Kernel launchers (each returns the launch status; nothing synchronises).
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
+cudaError_t pace_launch_decode_tc(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s);

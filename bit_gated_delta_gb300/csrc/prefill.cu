@@ -57,14 +57,7 @@ __device__ void store_quant_column(const PaceDev &st, long unit, int b, int h, c
     quant_group<G, BITS>(x, st.zero_point, uq, s, z);
 #pragma unroll
     for (int ww = 0; ww < WPG; ++ww) {
-      uint32_t word = 0;
-      if (BITS == 4) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) word |= (uq[8 * ww + t] | (uq[8 * ww + 4 + t] << 4)) << (8 * t);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) word |= uq[4 * ww + t] << (8 * t);
-      }
+      const uint32_t word = BITS == 4 ? pack_nibbles(uq + 8 * ww) : pack_bytes(uq + 4 * ww);
       codes[(g * WPG + ww) * D + j] = word;
     }
     st.scale[(unit * NG + g) * D + j] = __float2bfloat16_rn(s);

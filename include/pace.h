@@ -73,8 +73,8 @@ typedef struct pace_state pace_state;   /* opaque host handle */
 
 /* Byte offsets (from the state's device base) and strides of the resident arrays, for checkpoint
  * tooling and tests. Unused arrays have offset (size_t)-1. Units are u = b*H + h.
- *   codes4  uint32 [B][H4][d_k/8][d_v]  int4 heads: word (w, j) holds keys 8w..8w+7 of column j; byte t
- *                                      has key 8w+t in its low nibble and key 8w+4+t in its high nibble
+ *   codes4  uint32 [B][H4][d_k/8][d_v]  int4 heads: word (w, j) holds keys 8w..8w+7 of column j: key
+ *                                      8w+2s in bits 4s..4s+3, key 8w+2s+1 in bits 16+4s..19+4s (s=0..3)
  *   codes8  uint32 [B][H8][d_k/4][d_v]  int8 heads: byte t of word (w, j) holds key 4w+t of column j
  *           stored codes are unsigned: symmetric code c is stored as c+8 (int4) / c+128 (int8);
  *           zero-point codes are stored as they are
@@ -86,10 +86,11 @@ typedef struct pace_state pace_state;   /* opaque host handle */
  *   buf_v   int8   [B][H][dP][d_v]      mixed: bf16 values; fp32 buffer: float
  *   buf_s   float  [B][H][dP][4]        a_t, beta_t, key scale, value scale
  *   m       int32  [B][H]               tokens in the buffer
+ *   status  int32  [1]                  bit 0: a bounded device wait gave up (see pace_get_status)
  *   S       float/bf16 [B][H][d_k][d_v] state of PACE_STATE_FP32 / PACE_STATE_BF16
  * head_slot[h] is the index of head h inside its pool (codes4 or codes8). */
 typedef struct {
-  size_t codes4, codes8, scale, zp, buf_k, buf_v, buf_s, m, S;
+  size_t codes4, codes8, scale, zp, buf_k, buf_v, buf_s, m, S, status;
   size_t total_bytes;
   int H4, H8;
   int head_slot[PACE_MAX_HEADS];
@@ -158,6 +159,11 @@ pace_status pace_state_import(pace_state *state, const void *src, size_t bytes, 
  * this library actually keeps per state value (codes, scales, zero points, buffer, counters) * 8.
  * head_is_int8 as for pace_state_bytes. Returns a negative value for an invalid config. */
 double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, int literal_formula);
+
+/* Device-side status of a state: *status_out = 0, or bit 0 set when a bounded wait inside a kernel gave up
+ * (the unit involved was left unchanged). This call SYNCHRONISES `stream` to read the word; it returns
+ * PACE_ERR_TIMEOUT when the bit is set, and clears it when `clear` is non-zero. */
+pace_status pace_get_status(const pace_state *state, int clear, int *status_out, void *stream);
 
 /* Message for the last non-OK status returned to the calling thread ("" if none). */
 const char *pace_last_error(void);
