@@ -223,12 +223,20 @@ class PairRun:
         return read_blob(self.state)
 
     def codes_vs_oracle(self):
-        """(fraction of identical codes, max |difference|) over the sampled units."""
+        """(fraction of identical quantization levels, max |difference|) over the sampled units. The level is
+        the code itself for symmetric groups and code - zero point for zero-point groups: a near-tie that
+        flips a zero-point scale may move the stored code and the zero point together, while the represented
+        level moves by at most one step."""
         blob = self.blob()
+        zps = blob.zps() if self.wl.zero_point else None
         g, r = [], []
         for (b, h), u in self.units.items():
-            g.append(blob.codes(b, h))
-            r.append(u.code)
+            gc, rc = blob.codes(b, h), u.code
+            if zps is not None:
+                gc = gc - np.repeat(zps[b, h], self.wl.g, axis=0)
+                rc = rc - np.repeat(u.zp, self.wl.g, axis=0)
+            g.append(gc)
+            r.append(rc)
         return code_agreement(np.stack(g), np.stack(r))
 
     def state_vs_oracle(self) -> float:
