@@ -58,6 +58,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
   return true;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// Bulk (non-tensor) asynchronous copy global -> shared, completing `bytes` on the mbarrier. Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst_smem)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// Named barrier among the first `count` threads of the block (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void bar_sync_1(uint32_t count) { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); }
+
 // ---- descriptors ---------------------------------------------------------------------------------------
 // Shared-memory matrix descriptor, no swizzle: 8 x 16-byte core matrices (128 contiguous bytes each);
 // lbo / sbo are the byte distances between core matrices along the leading (K) and the strided (M or N)
