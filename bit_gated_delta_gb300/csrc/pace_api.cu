@@ -236,7 +236,7 @@ pace_status pace_decode_step(pace_state *state, const void *q, const void *k, co
   if (state->cfg.state_mode == PACE_STATE_BF16)
     e = pace_launch_decode_bf16(state->dev, io, cs);
   else if (state->cfg.state_mode == PACE_STATE_QUANT)
-    e = pace_launch_decode_tc(state->dev, io, 1, cs);
+    e = pace_launch_decode_quant(state->dev, io, 1, cs);
   else
     e = pace_launch_decode(state->dev, io, 1, cs);
   if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
@@ -249,7 +249,7 @@ pace_status pace_flush(pace_state *state, void *stream) {
   if (state->cfg.state_mode == PACE_STATE_BF16) return ok();   // no buffer
   PaceIO io{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_tc(state->dev, io, 0, cs)
+  cudaError_t e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_quant(state->dev, io, 0, cs)
                                                             : pace_launch_decode(state->dev, io, 0, cs);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
   return ok();
@@ -268,7 +268,7 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
   cudaError_t e = cudaSuccess;
   if (state->cfg.state_mode != PACE_STATE_BF16) {
     PaceIO fio{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-    e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_tc(state->dev, fio, 0, cs)
+    e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_quant(state->dev, fio, 0, cs)
                                                   : pace_launch_decode(state->dev, fio, 0, cs);   // pending buffers first
     if (e != cudaSuccess) return cuda_fail(e, "prefill flush launch");
   }

@@ -140,9 +140,9 @@ __device__ __forceinline__ float buffer_scale(float A, int qmax) {
 }
 
 // Stored-code extraction from packed words (layouts in pace.h). An int4 word holds keys 8w..8w+7 of one
-// column: key 8w+2s in bits 4s..4s+3 and key 8w+2s+1 in bits 16+4s..16+4s+3, so that masking the word
-// shifted by 4s with 0x000F000F yields the pair (key 2s, key 2s+1) in the two 16-bit halves.
-__device__ __forceinline__ int nibble_shift(int key_in_word) { return ((key_in_word & 1) << 4) | ((key_in_word >> 1) << 2); }
+// column in order, key 8w+e in bits 4e..4e+3; masking with 0x0F0F0F0F leaves the even keys as bytes and
+// 0xF0F0F0F0 the odd keys (times 16), the two planes the byte dot products use.
+__device__ __forceinline__ int nibble_shift(int key_in_word) { return key_in_word << 2; }
 __device__ __forceinline__ uint32_t nibble_of(uint32_t word, int key_in_word) {
   return (word >> nibble_shift(key_in_word)) & 0xFu;
 }
@@ -158,6 +158,62 @@ __device__ __forceinline__ uint32_t pack_bytes(const uint32_t *u) {
 }
 __device__ __forceinline__ uint32_t byte_of(uint32_t word, int key_in_word) {
   return (word >> (key_in_word << 3)) & 0xFFu;
+}
+
+// Requantize one key-axis group of G values (the arithmetic of quant_group) and write its packed words
+// to dst[0], dst[stride], ... as they are produced. Returns the bf16-exact scale and the zero point.
+template <int G, int BITS>
+__device__ __forceinline__ void quant_pack_group(const float (&x)[G], int zero_point, uint32_t *dst, int stride,
+                                                 float &s_out, int &z_out) {
+  constexpr int KPW = 32 / BITS;
+  float s;
+  int z;
+  if (!zero_point) {
+    constexpr int qmax = (1 << (BITS - 1)) - 1;
+    float A = 0.0f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) A = fmaxf(A, fabsf(x[i]));
+    s = bf16_round(__fdiv_rn(A, (float)qmax));
+    z = 1 << (BITS - 1);
+    if (!(s >= FLT_MIN)) s = 0.0f;
+  } else {
+    constexpr int qm = (1 << BITS) - 1;
+    float lo = 0.0f, hi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      lo = fminf(lo, x[i]);
+      hi = fmaxf(hi, x[i]);
+    }
+    s = bf16_round(__fdiv_rn(__fsub_rn(hi, lo), (float)qm));
+    z = 0;
+    if (!(s >= FLT_MIN)) {
+      s = 0.0f;
+    } else {
+      z = min(max(__float2int_rn(__fmul_rn(-lo, __fdiv_rn(1.0f, s))), 0), qm);
+    }
+  }
+  const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
+#pragma unroll
+  for (int w = 0; w < G / KPW; ++w) {
+    uint32_t u[KPW];
+#pragma unroll
+    for (int e = 0; e < KPW; ++e) {
+      int c;
+      if (s == 0.0f) {
+        c = z;                                     // symmetric: the offset (code 0); zero point: 0
+      } else if (!zero_point) {
+        constexpr int qmax = (1 << (BITS - 1)) - 1;
+        c = min(max(__float2int_rn(__fmul_rn(x[w * KPW + e], r)), -qmax), qmax) + z;
+      } else {
+        constexpr int qm = (1 << BITS) - 1;
+        c = min(max(__float2int_rn(__fmul_rn(x[w * KPW + e], r)) + z, 0), qm);
+      }
+      u[e] = (uint32_t)c;
+    }
+    dst[(size_t)w * stride] = BITS == 4 ? pack_nibbles(u) : pack_bytes(u);
+  }
+  s_out = s;
+  z_out = z;
 }
 
 }  // namespace pace

@@ -45,7 +45,7 @@ struct PaceIO {
 
 // Kernel launchers (each returns the launch status; nothing synchronises).
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
-cudaError_t pace_launch_decode_tc(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
+cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s);

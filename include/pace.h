@@ -73,8 +73,8 @@ typedef struct pace_state pace_state;   /* opaque host handle */
 
 /* Byte offsets (from the state's device base) and strides of the resident arrays, for checkpoint
  * tooling and tests. Unused arrays have offset (size_t)-1. Units are u = b*H + h.
- *   codes4  uint32 [B][H4][d_k/8][d_v]  int4 heads: word (w, j) holds keys 8w..8w+7 of column j: key
- *                                      8w+2s in bits 4s..4s+3, key 8w+2s+1 in bits 16+4s..19+4s (s=0..3)
+ *   codes4  uint32 [B][H4][d_k/8][d_v]  int4 heads: word (w, j) holds keys 8w..8w+7 of column j, key
+ *                                      8w+e in bits 4e..4e+3
  *   codes8  uint32 [B][H8][d_k/4][d_v]  int8 heads: byte t of word (w, j) holds key 4w+t of column j
  *           stored codes are unsigned: symmetric code c is stored as c+8 (int4) / c+128 (int8);
  *           zero-point codes are stored as they are

@@ -51,9 +51,8 @@ class Blob:
         if not is8:
             w = self._arr(self.L.codes4, np.uint32, (self.B, self.L.H4, D // 8, D))[b, slot]
             out = np.zeros((D, D), np.int32)
-            for s2 in range(4):
-                out[np.arange(D // 8) * 8 + 2 * s2] = (w >> (4 * s2)) & 0xF
-                out[np.arange(D // 8) * 8 + 2 * s2 + 1] = (w >> (16 + 4 * s2)) & 0xF
+            for e in range(8):
+                out[np.arange(D // 8) * 8 + e] = (w >> (4 * e)) & 0xF
             off = 8
         else:
             w = self._arr(self.L.codes8, np.uint32, (self.B, self.L.H8, D // 4, D))[b, slot]
