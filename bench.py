@@ -141,7 +141,7 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode.cu", "bit_gated_delta_gb300/csrc/pace_common.cuh",
+DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode_mma.cu", "bit_gated_delta_gb300/csrc/pace_common.cuh",
                   "bit_gated_delta_gb300/csrc/pace_internal.h"]
 
 
@@ -403,11 +403,11 @@ def main():
     units = wl.B * wl.H
     alg = units * decode_bytes_period_avg(wl.d_k, wl.g, wl.dP)
     achieved = alg / (ms * 1e-3) / 1e9
-    traffic = recorded_traffic("decode_kernel", f"pace4_b{wl.B}")
+    traffic = recorded_traffic("decode_mma_kernel", f"pace4_b{wl.B}")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_kernel<128,64>",
+                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_mma_kernel<128,64,4>",
                 "algorithmic_bytes_per_launch": alg,
-                "note": "one decode_kernel launch per step; duration = event time of K graph-replayed steps / K"}
+                "note": "one decode_mma_kernel launch per step; duration = event time of K graph-replayed steps / K"}
     e2e = time_e2e(torch, P, setup, K)
     e2e["value"] *= world
     prefill = {"tokens": setup.prefill_tokens, "ms": setup.prefill_ms,

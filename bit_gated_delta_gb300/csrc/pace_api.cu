@@ -197,6 +197,7 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
   for (int h = 0; h < cfg->n_heads; ++h) {
     d.head_is_int8[h] = L.head_is_int8[h];
     d.head_slot[h] = (int16_t)L.head_slot[h];
+    d.pool_head[(L.head_is_int8[h] ? L.H4 : 0) + L.head_slot[h]] = (int16_t)h;
   }
   // zero state: every code stands for 0 (symmetric codes are stored offset by 2^(b-1))
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -204,7 +205,10 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
   if (e == cudaSuccess && cfg->state_mode == PACE_STATE_QUANT && !cfg->zero_point) {
     const size_t D = cfg->d_k;
     if (L.H4) e = cudaMemsetAsync(d.codes4, 0x88, (size_t)batch * L.H4 * (D / 8) * D * 4, cs);
-    if (e == cudaSuccess && L.H8) e = cudaMemsetAsync(d.codes8, 0x80, (size_t)batch * L.H8 * (D / 4) * D * 4, cs);
+    // int8 code 0 is stored as 128: low-nibble plane 0x0, high-nibble plane 0x8
+    const size_t plane = (size_t)(D / 8) * D * 4;
+    if (e == cudaSuccess && L.H8)
+      e = cudaMemset2DAsync(reinterpret_cast<char *>(d.codes8) + plane, 2 * plane, 0x88, plane, (size_t)batch * L.H8, cs);
   }
   if (e != cudaSuccess) {
     delete s;

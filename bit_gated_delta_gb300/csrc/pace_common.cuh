@@ -139,33 +139,34 @@ __device__ __forceinline__ float buffer_scale(float A, int qmax) {
   return __fdiv_rn(A, (float)qmax);
 }
 
-// Stored-code extraction from packed words (layouts in pace.h). An int4 word holds keys 8w..8w+7 of one
-// column in order, key 8w+e in bits 4e..4e+3; masking with 0x0F0F0F0F leaves the even keys as bytes and
-// 0xF0F0F0F0 the odd keys (times 16), the two planes the byte dot products use.
-__device__ __forceinline__ int nibble_shift(int key_in_word) { return key_in_word << 2; }
-__device__ __forceinline__ uint32_t nibble_of(uint32_t word, int key_in_word) {
-  return (word >> nibble_shift(key_in_word)) & 0xFu;
+// ---- Packed code layout (pace.h), in the order of the warp-level MMA fragments. Column j has
+// mt = j/16, r8 = j%8, hi = (j/8)%2; key i has n = i/8, t = (i%8)/2, odd = i%2, p = n/4, r = n%4. Word
+// (column j, lane r8*4+t, p) holds the keys 8n+2t, 8n+2t+1 of the four 8-key blocks n = 4p..4p+3: key
+// 8n+2t in bits 4r..4r+3, key 8n+2t+1 in bits 16+4r..19+4r, so that (word >> 4r) & 0x000F000F is that
+// pair in two 16-bit halves. Word index = ((mt*(D/64) + p/2)*32 + r8*4+t)*4 + hi*2 + p%2: one lane's
+// four words of 64 keys are one 16-byte vector, and a warp reads 512 contiguous bytes per (mt, p/2).
+// int8 codes are two such planes: plane 0 holds the low nibbles, plane 1 the high nibbles.
+__host__ __device__ __forceinline__ uint32_t code_word(int D, int j, int i) {
+  const int mt = j >> 4, r8 = j & 7, hi = (j >> 3) & 1, t = (i >> 1) & 3, p = i >> 5;
+  return (uint32_t)((((mt * (D >> 6) + (p >> 1)) * 32 + r8 * 4 + t) << 2) + hi * 2 + (p & 1));
 }
-// Pack 8 stored int4 codes (keys 0..7 of a word) / 4 stored int8 codes.
-__device__ __forceinline__ uint32_t pack_nibbles(const uint32_t *u) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) w |= u[e] << nibble_shift(e);
-  return w;
-}
-__device__ __forceinline__ uint32_t pack_bytes(const uint32_t *u) {
-  return u[0] | (u[1] << 8) | (u[2] << 16) | (u[3] << 24);
-}
-__device__ __forceinline__ uint32_t byte_of(uint32_t word, int key_in_word) {
-  return (word >> (key_in_word << 3)) & 0xFFu;
+__host__ __device__ __forceinline__ uint32_t code_plane_words(int D) { return (uint32_t)(D * D / 8); }
+__host__ __device__ __forceinline__ int nibble_shift(int i) { return (((i >> 3) & 3) << 2) | ((i & 1) << 4); }
+// Stored code (unsigned) of key i of column j; BITS 4 or 8 (two nibble planes).
+template <int BITS>
+__device__ __forceinline__ uint32_t load_code(const uint32_t *unit_codes, int D, int j, int i) {
+  const uint32_t wi = code_word(D, j, i);
+  const int sh = nibble_shift(i);
+  const uint32_t lo = (unit_codes[wi] >> sh) & 0xFu;
+  if (BITS == 4) return lo;
+  return lo | (((unit_codes[code_plane_words(D) + wi] >> sh) & 0xFu) << 4);
 }
 
-// Requantize one key-axis group of G values (the arithmetic of quant_group) and write its packed words
-// to dst[0], dst[stride], ... as they are produced. Returns the bf16-exact scale and the zero point.
+// Requantize one key-axis group of G values (keys g*G .. g*G+G-1 of column j) with the arithmetic of
+// quant_group and store the packed codes of the group. Returns the bf16-exact scale and the zero point.
 template <int G, int BITS>
-__device__ __forceinline__ void quant_pack_group(const float (&x)[G], int zero_point, uint32_t *dst, int stride,
-                                                 float &s_out, int &z_out) {
-  constexpr int KPW = 32 / BITS;
+__device__ __forceinline__ void quant_store_group(const float (&x)[G], int zero_point, uint32_t *unit_codes, int D,
+                                                  int j, int g, float &s_out, int &z_out) {
   float s;
   int z;
   if (!zero_point) {
@@ -193,24 +194,38 @@ __device__ __forceinline__ void quant_pack_group(const float (&x)[G], int zero_p
     }
   }
   const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
+  uint32_t u[G];
 #pragma unroll
-  for (int w = 0; w < G / KPW; ++w) {
-    uint32_t u[KPW];
-#pragma unroll
-    for (int e = 0; e < KPW; ++e) {
-      int c;
-      if (s == 0.0f) {
-        c = z;                                     // symmetric: the offset (code 0); zero point: 0
-      } else if (!zero_point) {
-        constexpr int qmax = (1 << (BITS - 1)) - 1;
-        c = min(max(__float2int_rn(__fmul_rn(x[w * KPW + e], r)), -qmax), qmax) + z;
-      } else {
-        constexpr int qm = (1 << BITS) - 1;
-        c = min(max(__float2int_rn(__fmul_rn(x[w * KPW + e], r)) + z, 0), qm);
-      }
-      u[e] = (uint32_t)c;
+  for (int e = 0; e < G; ++e) {
+    int c;
+    if (s == 0.0f) {
+      c = z;                                     // symmetric: the offset (code 0); zero point: 0
+    } else if (!zero_point) {
+      constexpr int qmax = (1 << (BITS - 1)) - 1;
+      c = min(max(__float2int_rn(__fmul_rn(x[e], r)), -qmax), qmax) + z;
+    } else {
+      constexpr int qm = (1 << BITS) - 1;
+      c = min(max(__float2int_rn(__fmul_rn(x[e], r)) + z, 0), qm);
     }
-    dst[(size_t)w * stride] = BITS == 4 ? pack_nibbles(u) : pack_bytes(u);
+    u[e] = (uint32_t)c;
+  }
+  // the group covers whole words: G/32 spans of 32 keys, four words (t = 0..3) each
+#pragma unroll
+  for (int pw = 0; pw < G / 32; ++pw) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int e0 = pw * 32 + rr * 8 + 2 * t;      // key offset inside the group
+        const int sh = 4 * rr;
+        lo |= ((u[e0] & 0xFu) << sh) | ((u[e0 + 1] & 0xFu) << (16 + sh));
+        hi |= (((u[e0] >> 4) & 0xFu) << sh) | (((u[e0 + 1] >> 4) & 0xFu) << (16 + sh));
+      }
+      const uint32_t wi = code_word(D, j, g * G + pw * 32 + 2 * t);
+      unit_codes[wi] = lo;
+      if (BITS == 8) unit_codes[code_plane_words(D) + wi] = hi;
+    }
   }
   s_out = s;
   z_out = z;

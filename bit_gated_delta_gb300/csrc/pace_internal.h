@@ -24,6 +24,7 @@ struct PaceDev {
   void *S;                 // f32 / bf16 [B][H][D][D]
   uint8_t head_is_int8[PACE_MAX_HEADS];
   int16_t head_slot[PACE_MAX_HEADS];
+  int16_t pool_head[PACE_MAX_HEADS];   // heads of the int4 pool in slot order, then those of the int8 pool
 };
 
 struct pace_state {

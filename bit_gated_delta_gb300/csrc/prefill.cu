@@ -16,25 +16,26 @@ __host__ __device__ inline size_t prefill_smem_bytes(int D) {
   return (size_t)D * D * 4 + 2 * (size_t)PF_STAGE * D * 4 + 2 * PF_STAGE * 4;
 }
 
+// Resident codes of unit (b, h): int4 heads one plane, int8 heads two nibble planes (layout in pace.h).
+template <int D, int BITS>
+__device__ __forceinline__ uint32_t *unit_codes(const PaceDev &st, int b, int h) {
+  return BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
+                   : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
+}
+
 // fp32 column j of the resident state into S_s[i][j].
 template <int D, int G, int BITS>
 __device__ void load_quant_column(const PaceDev &st, long unit, int b, int h, float *S_s) {
-  constexpr int KPW = 32 / BITS, NWC = D / KPW, NG = D / G;
+  constexpr int NG = D / G;
   const int j = threadIdx.x;
-  const uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * NWC * D
-                                    : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * NWC * D;
-#pragma unroll
+  const uint32_t *codes = unit_codes<D, BITS>(st, b, h);
+#pragma unroll 1
   for (int g = 0; g < NG; ++g) {
     const float s = __bfloat162float(st.scale[(unit * NG + g) * D + j]);
     const int z = st.zero_point ? (int)st.zp[(unit * NG + g) * D + j] : (1 << (BITS - 1));
-#pragma unroll
-    for (int ww = 0; ww < G / KPW; ++ww) {
-      const uint32_t w = codes[(g * (G / KPW) + ww) * D + j];
-#pragma unroll
-      for (int t = 0; t < KPW; ++t) {
-        const uint32_t u = BITS == 4 ? nibble_of(w, t) : byte_of(w, t);
-        S_s[((g * (G / KPW) + ww) * KPW + t) * D + j] = s * (float)((int)u - z);
-      }
+    for (int ii = 0; ii < G; ++ii) {
+      const int i = g * G + ii;
+      S_s[i * D + j] = s * (float)((int)load_code<BITS>(codes, D, j, i) - z);
     }
   }
 }
@@ -42,24 +43,17 @@ __device__ void load_quant_column(const PaceDev &st, long unit, int b, int h, fl
 // Round column j of S_s once and store it in the resident format.
 template <int D, int G, int BITS>
 __device__ void store_quant_column(const PaceDev &st, long unit, int b, int h, const float *S_s) {
-  constexpr int KPW = 32 / BITS, NWC = D / KPW, NG = D / G, WPG = G / KPW;
+  constexpr int NG = D / G;
   const int j = threadIdx.x;
-  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * NWC * D
-                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * NWC * D;
-#pragma unroll
+  uint32_t *codes = unit_codes<D, BITS>(st, b, h);
+#pragma unroll 1
   for (int g = 0; g < NG; ++g) {
     float x[G];
 #pragma unroll
     for (int ii = 0; ii < G; ++ii) x[ii] = S_s[(g * G + ii) * D + j];
-    uint32_t uq[G];
     float s;
     int z;
-    quant_group<G, BITS>(x, st.zero_point, uq, s, z);
-#pragma unroll
-    for (int ww = 0; ww < WPG; ++ww) {
-      const uint32_t word = BITS == 4 ? pack_nibbles(uq + 8 * ww) : pack_bytes(uq + 4 * ww);
-      codes[(g * WPG + ww) * D + j] = word;
-    }
+    quant_store_group<G, BITS>(x, st.zero_point, codes, D, j, g, s, z);
     st.scale[(unit * NG + g) * D + j] = __float2bfloat16_rn(s);
     if (st.zero_point) st.zp[(unit * NG + g) * D + j] = (uint8_t)z;
   }

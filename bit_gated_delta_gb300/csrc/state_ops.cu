@@ -8,26 +8,25 @@
 
 namespace pace {
 
+template <int D, int BITS>
+__device__ __forceinline__ uint32_t *unit_codes(const PaceDev &st, int b, int h) {
+  return BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
+                   : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
+}
+
 template <int D, int G, int BITS>
 __device__ void quantize_column(const PaceDev &st, long unit, int b, int h, const float *Sg) {
-  constexpr int KPW = 32 / BITS, NWC = D / KPW, NG = D / G, WPG = G / KPW;
+  constexpr int NG = D / G;
   const int j = threadIdx.x;
-  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * NWC * D
-                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * NWC * D;
-#pragma unroll
+  uint32_t *codes = unit_codes<D, BITS>(st, b, h);
+#pragma unroll 1
   for (int g = 0; g < NG; ++g) {
     float x[G];
 #pragma unroll
     for (int ii = 0; ii < G; ++ii) x[ii] = Sg[(g * G + ii) * D + j];
-    uint32_t uq[G];
     float s;
     int z;
-    quant_group<G, BITS>(x, st.zero_point, uq, s, z);
-#pragma unroll
-    for (int ww = 0; ww < WPG; ++ww) {
-      const uint32_t word = BITS == 4 ? pack_nibbles(uq + 8 * ww) : pack_bytes(uq + 4 * ww);
-      codes[(g * WPG + ww) * D + j] = word;
-    }
+    quant_store_group<G, BITS>(x, st.zero_point, codes, D, j, g, s, z);
     st.scale[(unit * NG + g) * D + j] = __float2bfloat16_rn(s);
     if (st.zero_point) st.zp[(unit * NG + g) * D + j] = (uint8_t)z;
   }
@@ -35,17 +34,14 @@ __device__ void quantize_column(const PaceDev &st, long unit, int b, int h, cons
 
 template <int D, int G, int BITS>
 __device__ void dequantize_column(const PaceDev &st, long unit, int b, int h, float *So) {
-  constexpr int KPW = 32 / BITS, NWC = D / KPW, NG = D / G;
+  constexpr int NG = D / G;
   const int j = threadIdx.x;
-  const uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * NWC * D
-                                    : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * NWC * D;
+  const uint32_t *codes = unit_codes<D, BITS>(st, b, h);
   for (int i = 0; i < D; ++i) {
     const int g = i / G;
     const float s = __bfloat162float(st.scale[(unit * NG + g) * D + j]);
     const int z = st.zero_point ? (int)st.zp[(unit * NG + g) * D + j] : (1 << (BITS - 1));
-    const uint32_t w = codes[(i / KPW) * D + j];
-    const uint32_t u = BITS == 4 ? nibble_of(w, i % KPW) : byte_of(w, i % KPW);
-    So[i * D + j] = s * (float)((int)u - z);
+    So[i * D + j] = s * (float)((int)load_code<BITS>(codes, D, j, i) - z);
   }
 }
 

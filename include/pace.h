@@ -73,9 +73,13 @@ typedef struct pace_state pace_state;   /* opaque host handle */
 
 /* Byte offsets (from the state's device base) and strides of the resident arrays, for checkpoint
  * tooling and tests. Unused arrays have offset (size_t)-1. Units are u = b*H + h.
- *   codes4  uint32 [B][H4][d_k/8][d_v]  int4 heads: word (w, j) holds keys 8w..8w+7 of column j, key
- *                                      8w+e in bits 4e..4e+3
- *   codes8  uint32 [B][H8][d_k/4][d_v]  int8 heads: byte t of word (w, j) holds key 4w+t of column j
+ *   codes4  uint32 [B][H4][d_k*d_v/8]   int4 heads, in warp-level MMA fragment order. For column j let
+ *                                      mt = j/16, r8 = j%8, hi = (j/8)%2; for key i let n = i/8,
+ *                                      t = (i%8)/2, p = n/4, r = n%4. Key i of column j is the nibble at
+ *                                      bit 4r + 16*(i%2) of word ((mt*(d_k/64) + p/2)*32 + r8*4 + t)*4
+ *                                      + hi*2 + p%2
+ *   codes8  uint32 [B][H8][2][d_k*d_v/8] int8 heads: plane 0 = low nibbles, plane 1 = high nibbles, each
+ *                                      in the codes4 arrangement
  *           stored codes are unsigned: symmetric code c is stored as c+8 (int4) / c+128 (int8);
  *           zero-point codes are stored as they are
  *   scale   bf16   [B][H][d_k/g][d_v]   group scales

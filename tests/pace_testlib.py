@@ -43,23 +43,31 @@ class Blob:
     def zps(self):
         return self._arr(self.L.zp, np.uint8, (self.B, self.H, self.NG, self.D)).astype(np.int32)
 
+    def word_index(self, j: np.ndarray, i: np.ndarray) -> np.ndarray:
+        """Index of the word holding key i of column j in a unit's code plane (fragment order, pace.h)."""
+        mt, r8, hi = j >> 4, j & 7, (j >> 3) & 1
+        t, p = (i >> 1) & 3, i >> 5
+        return ((mt * (self.D // 64) + (p >> 1)) * 32 + r8 * 4 + t) * 4 + hi * 2 + (p & 1)
+
     def codes(self, b: int, h: int) -> np.ndarray:
         """Canonical codes [d_k][d_v] of unit (b, h), as the oracle writes them."""
         D = self.D
         is8 = bool(self.L.head_is_int8[h])
         slot = self.L.head_slot[h]
+        npl = D * D // 8
         if not is8:
-            w = self._arr(self.L.codes4, np.uint32, (self.B, self.L.H4, D // 8, D))[b, slot]
-            out = np.zeros((D, D), np.int32)
-            for e in range(8):
-                out[np.arange(D // 8) * 8 + e] = (w >> (4 * e)) & 0xF
-            off = 8
+            planes = [self._arr(self.L.codes4, np.uint32, (self.B, self.L.H4, npl))[b, slot]]
         else:
-            w = self._arr(self.L.codes8, np.uint32, (self.B, self.L.H8, D // 4, D))[b, slot]
-            out = np.zeros((D, D), np.int32)
-            for t in range(4):
-                out[np.arange(D // 4) * 4 + t] = (w >> (8 * t)) & 0xFF
-            off = 128
+            p2 = self._arr(self.L.codes8, np.uint32, (self.B, self.L.H8, 2, npl))[b, slot]
+            planes = [p2[0], p2[1]]
+        i = np.arange(D)[:, None]
+        j = np.arange(D)[None, :]
+        wi = self.word_index(j, i)
+        shift = (((i >> 3) & 3) << 2) | ((i & 1) << 4)
+        out = ((planes[0][wi] >> shift) & 0xF).astype(np.int32)
+        if is8:
+            out |= (((planes[1][wi] >> shift) & 0xF).astype(np.int32) << 4)
+        off = 128 if is8 else 8
         return out if self.cfg.zero_point else out - off
 
     def buffer(self, b: int, h: int):
