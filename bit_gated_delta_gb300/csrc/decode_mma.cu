@@ -1,24 +1,31 @@
 // PACE decode step with fused flush, quantized state ([P1] 어떻게 동작하나: round once every dP tokens, the
 // buffered tokens applied together at the flush; [P2] 1. Key Terms & Definitions: the gated delta rule).
 //
-// One warp per unit (sequence b, head h); the warp walks the state in blocks of 32 columns. Both dense
-// contractions of the step run on the tensor cores as warp-level bf16 MMAs (m16n8k16 / m16n8k8, fp32
-// accumulation), with operands built in registers straight from the packed codes:
-//   dots   D_g[v][j] = sum_{i in group g} B[v][i] (128 + u_ij)        M = vectors v, N = columns j, K = keys
-//          The vectors are the int8 key codes of the buffered tokens and three int8 digits of a 24-bit
-//          fixed-point image of q. The packed words are stored in fragment order (pace.h): the lane's
-//          word gives its B fragment as (word >> 4r) & 0x000F000F | 0x43004300, the bf16 pair
-//          (128 + u, 128 + u'). Every product and partial sum is an exact integer in fp32, so with the
-//          group scale s_gj and zero point z_gj: (S_hat^T x)_j = sum_g s_gj (D_g[v][j] - (128 + z_gj) c_vg),
-//          c_vg = sum_{i in g} B[v][i];
-//   flush  S_new^T[j][i] = G_m s_gj (u_ij - z_gj) + sum_s (rho_s u_s,j) k_s,i  M = columns, N = keys,
+// One warp per unit (sequence b, head h); the warp walks the state in blocks of 32 columns. Every dense
+// contraction of the step runs on the tensor cores as a warp-level MMA (fp32 accumulation), with operands
+// built in registers straight from the packed codes:
+//   dots   D_g[v][j] = sum_{i in group g} A[v][i] B[i][j]        M = vectors v, N = columns j, K = keys
+//          fp16 operands. The vectors are the int8 key codes of the buffered tokens and three int8 digits
+//          of a 24-bit fixed-point image of q, kept as swizzled fp16 rows read with ldmatrix. The packed
+//          words are stored in fragment order (pace.h): a lane's word w gives its B fragment of a 16-key
+//          step as (w & 0x000F000F) | 0x64006400 (the pair 1024 + u) for the first 8 keys and
+//          (w & 0x00F000F0) | 0x64006400 (1024 + 16u) for the last 8, whose A values are pre-scaled by
+//          1/16. Every product and partial sum is an exact integer or sixteenth in fp32, so with the group
+//          scale s_gj and zero point z_gj:
+//            (S_hat^T x)_j = sum_g s_gj (D_g[v][j] - T1_vg - z_gj T2_vg),
+//            T1 = 1024 (sum of the first-half A) + 1024 (sum of the second-half A), T2 = sum of x over g;
+//   tables the Gram products k_s.k_t, the products k_s.(q digits) and the group sums T1, T2 are MMAs of
+//          the same fp16 rows;
+//   flush  S_new^T[j][i] = sum_s (rho_s u_s,j) k_s,i + G_m s_gj (u_ij - z_gj)   M = columns, N = keys,
 //          K = (token, part): rho_s u_s,j is split into three bf16 parts (fp32-accurate) and the int8 keys
-//          are exact in bf16. The accumulator starts from the dequantized state, and a lane's fragment
-//          holds exactly the keys of its own packed words: each key-axis group is requantized by the lane
+//          are exact in bf16. A lane's accumulator fragment holds exactly the keys of its own packed
+//          words: the old state is added in fp32 pairs, each key-axis group is requantized by the lane
 //          quad that holds it (two shuffles for the absmax or the min/max) and written back in place.
 // Between the two, each lane replays one column in reduced form (fp32):
 //   u_t = beta_t (v_t - G_t (S_hat^T k_t) - sum_{s<t} (G_t/G_s)(k_s.k_t) u_s),   G_t = a_1 .. a_t
 //   o   = G_m (S_hat^T q) + sum_s (G_m/G_s)(k_s.q) u_s
+#include <cuda_fp16.h>
+
 #include "pace_common.cuh"
 
 namespace pace {
@@ -27,32 +34,49 @@ constexpr int DM_WARPS = 4;   // units (warps) per block
 constexpr int PB_STRIDE = 40; // floats per row of the per-block dot table (conflict-free fragment stores)
 constexpr int UB_STRIDE = 36; // floats per row of the per-block replay table (conflict-free fragment loads)
 
+// RN(1/(1 + i/128)), i < 128: the reciprocals of the 8-bit significands of bf16 scales. Each entry is the
+// correctly rounded double quotient rounded to float; no quotient 128/(128+i) lies within 2^-53 of a float
+// rounding tie, so the double rounding is exact.
+struct RcpTable {
+  float v[128];
+};
+constexpr RcpTable make_rcp_table() {
+  RcpTable t{};
+  for (int i = 0; i < 128; ++i) t.v[i] = (float)(128.0 / (128 + i));
+  return t;
+}
+__device__ const RcpTable g_rcp = make_rcp_table();
+
 __host__ __device__ inline int dm_dpp(int dP) { return 8 * ((dP + 7) / 8); }   // token slots per K part
+__host__ __device__ inline int dm_wstride(int dP) { return dP <= 8 ? 8 : dP; }
+__host__ __device__ inline int dm_nvt(int dP) { return (dP + 3 + 15) / 16; }   // 16-vector tiles
 
 struct MmaSmem {
-  size_t krow, vrow, abf, kbf, pb, ub, W, a, gam, dmq, cq, ck, vsc, bt, sv, csum, total;
+  size_t krow, vrow, ah, kbf, pb, ub, W, tk, ck, cf, a, vsc, gam, dmq, ssc, szp, total;
 };
 // Per-warp work area.
-__host__ __device__ inline MmaSmem mma_smem(int D, int dP, int mixed) {
+__host__ __device__ inline MmaSmem mma_smem(int D, int G, int dP, int mixed, int zp) {
   MmaSmem L;
   size_t off = 0;
-  const int nvmax = dP + 3, nvt = (nvmax + 15) / 16;
+  const int nvmax = dP + 3, nrow = 16 * dm_nvt(dP), ws = dm_wstride(dP);
   L.krow = carve(off, (size_t)nvmax * D);                 // int8 key rows, then the three digits of q
   L.vrow = carve(off, (size_t)dP * D * (mixed ? 2 : 1));  // value codes (int8) or bf16 values
-  L.abf = carve(off, (size_t)nvt * (D / 16) * 32 * 16);   // A fragments of the vectors (bf16)
+  L.ah = carve(off, (size_t)nrow * D * 2);                // fp16 rows of the vectors, 16-byte chunks
+                                                          // XOR-swizzled by row (also staging)
   L.kbf = carve(off, (size_t)D * dm_dpp(dP) * 2);          // flush B operand: bf16 k_s,i as [i][s]
-  L.pb = carve(off, (size_t)nvmax * PB_STRIDE * 4);       // dots of one 32-column block [v][j]
+  L.pb = carve(off, (size_t)nvmax * PB_STRIDE * 4);       // dots of one 32-column block [v][j]; while the
+                                                          // tables are built: G_t/G_s, then k_s.(q digit d)
   L.ub = carve(off, (size_t)dP * UB_STRIDE * 4);          // replayed u of one block [s][j]
-  L.W = carve(off, (size_t)dP * dP * 4);
+  L.W = carve(off, (size_t)ws * dP * 4);                  // (G_t/G_s) s_ks s_kt (k_s.k_t)
+  L.tk = carve(off, (size_t)dP * 16);                     // per token: G_t s_kt, beta_t, s_vt, readout coef
+  L.ck = carve(off, (size_t)dP * 4);                      // flush coefficient (G_m/G_s) s_ks
+  L.cf = carve(off, (size_t)nrow * 4 * 8);                // (T1, T2) per vector and group
   L.a = carve(off, (size_t)dP * 4);
+  L.vsc = carve(off, (size_t)nvmax * 4);
   L.gam = carve(off, (size_t)dP * 4);
   L.dmq = carve(off, (size_t)dP * 4);
-  L.cq = carve(off, (size_t)dP * 4);
-  L.ck = carve(off, (size_t)dP * 4);
-  L.vsc = carve(off, (size_t)nvmax * 4);
-  L.bt = carve(off, (size_t)dP * 4);
-  L.sv = carve(off, (size_t)dP * 4);
-  L.csum = carve(off, (size_t)nvmax * 4 * 4);
+  L.ssc = carve(off, (size_t)(D / G) * D * 2);            // the unit's group scales (bf16), as resident
+  L.szp = carve(off, zp ? (size_t)(D / G) * D : 0);       // and zero points
   L.total = carve(off, 0, 16);
   return L;
 }
@@ -60,44 +84,84 @@ __host__ __device__ inline MmaSmem mma_smem(int D, int dP, int mixed) {
 struct MmaShared {
   int8_t *krow;
   unsigned char *vrow;
-  uint4 *abf;
+  __half *ah;
   uint32_t *kbf;
-  float *pb, *ub, *W, *a, *gam, *dmq, *cq, *ck, *vsc, *bt, *sv;
-  int *csum;
+  float *pb, *ub, *W, *dmt;
+  float4 *tk;
+  float *ck;
+  float2 *cf;
+  float *e3, *a, *vsc, *gam, *dmq;
+  __nv_bfloat16 *ssc;
+  uint8_t *szp;
 };
-__device__ inline MmaShared mma_shared(unsigned char *base, const MmaSmem &L) {
+__device__ inline MmaShared mma_shared(unsigned char *base, const MmaSmem &L, int dP) {
   MmaShared s;
   s.krow = reinterpret_cast<int8_t *>(base + L.krow);
   s.vrow = base + L.vrow;
-  s.abf = reinterpret_cast<uint4 *>(base + L.abf);
+  s.ah = reinterpret_cast<__half *>(base + L.ah);
   s.kbf = reinterpret_cast<uint32_t *>(base + L.kbf);
   s.pb = reinterpret_cast<float *>(base + L.pb);
   s.ub = reinterpret_cast<float *>(base + L.ub);
   s.W = reinterpret_cast<float *>(base + L.W);
+  s.dmt = s.pb;                                           // G_t/G_s, while the tables are built
+  s.e3 = s.pb + dm_wstride(dP) * dP;                      // k_s . (q digit d), likewise
+  s.tk = reinterpret_cast<float4 *>(base + L.tk);
+  s.ck = reinterpret_cast<float *>(base + L.ck);
+  s.cf = reinterpret_cast<float2 *>(base + L.cf);
   s.a = reinterpret_cast<float *>(base + L.a);
+  s.vsc = reinterpret_cast<float *>(base + L.vsc);
   s.gam = reinterpret_cast<float *>(base + L.gam);
   s.dmq = reinterpret_cast<float *>(base + L.dmq);
-  s.cq = reinterpret_cast<float *>(base + L.cq);
-  s.ck = reinterpret_cast<float *>(base + L.ck);
-  s.vsc = reinterpret_cast<float *>(base + L.vsc);
-  s.bt = reinterpret_cast<float *>(base + L.bt);
-  s.sv = reinterpret_cast<float *>(base + L.sv);
-  s.csum = reinterpret_cast<int *>(base + L.csum);
+  s.ssc = reinterpret_cast<__nv_bfloat16 *>(base + L.ssc);
+  s.szp = base + L.szp;
   return s;
 }
 
-// D (4 fp32) += A (16x16 bf16, 4 regs) x B (16x8 bf16, 2 regs)
-__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// ---- warp-level MMAs (fp32 accumulators) ----------------------------------------------------------------
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D = A x B (zero accumulator)
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// D (4 fp32) += A (16x8 bf16, 2 regs) x B (8x8 bf16, 1 reg)
-__device__ __forceinline__ void mma8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+__device__ __forceinline__ void mma_bf16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+__device__ __forceinline__ void mma8_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
   asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(b0));
 }
+// Fragments of 8x8 b16 tiles from shared memory (row addresses from lanes 0-7, 8-15, 16-23, 24-31).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"((uint32_t)__cvta_generic_to_shared(p))
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"((uint32_t)__cvta_generic_to_shared(p))
+               : "memory");
+}
+
+// Element offset of 16-byte chunk c of fp16 row r (D halves per row): chunks are XOR-swizzled by r mod 8
+// so that the 8 row addresses of one ldmatrix tile fall in distinct banks.
+template <int D>
+__device__ __forceinline__ int ah_off(int r, int c) { return r * D + ((c ^ (r & 7)) << 3); }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -106,23 +170,57 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
-// bf16 pair (128 + u, 128 + u') of the nibbles at bits 4r and 16 + 4r of a packed word.
-__device__ __forceinline__ uint32_t nib_pair(uint32_t word, int r) {
-  return ((word >> (4 * r)) & 0x000F000Fu) | 0x43004300u;
+// fp16 pair of two signed int8 codes (bytes selected from x by `sel`), times 1 or 1/16; exact.
+// (code + 128) | 0x6400 is the fp16 number 1152 + code.
+__device__ __forceinline__ uint32_t i8pair_f16(uint32_t x, uint32_t sel, bool sixteenth) {
+  const uint32_t h = (__byte_perm(x, 0u, sel) ^ 0x00800080u) | 0x64006400u;
+  const __half2 v = *reinterpret_cast<const __half2 *>(&h);
+  const __half2 r = sixteenth ? __hfma2(v, __float2half2_rn(0.0625f), __float2half2_rn(-72.0f))
+                              : __hsub2(v, __float2half2_rn(1152.0f));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t f16x2_scale(uint32_t p, float f) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2 *>(&p), __float2half2_rn(f));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// bf16(fl(num / den)) for num >= 0: a product with rc = fl(1/den) is within two ulps of the quotient, so it
+// rounds to the same bf16 unless it lies within three ulps of a bf16 rounding tie; then the exact quotient.
+__device__ __forceinline__ float bf16_quot(float num, float den, float rc) {
+  float q = __fmul_rn(num, rc);
+  if ((__float_as_uint(q) & 0xFFFFu) - 0x7FFDu <= 6u) q = __fdiv_rn(num, den);
+  return bf16_round(q);
+}
+// RN(1/s) for a positive normal s with an 8-bit significand: the table entry of the significand, with the
+// power of two applied exactly to the exponent (far out of range: the division itself).
+__device__ __forceinline__ float rcp_bf16(float s) {
+  const uint32_t b = __float_as_uint(s), e = b >> 23;
+  if (e > 252u) return __fdiv_rn(1.0f, s);
+  return __uint_as_float(__float_as_uint(__ldg(&g_rcp.v[(b >> 16) & 0x7Fu])) + ((127u - e) << 23));
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-
-template <int D, int BITS>
-__device__ __forceinline__ uint32_t *dm_unit_codes(const PaceDev &st, int b, int h) {
-  return BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
-                   : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)), "l"(src)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <int CPL>
-__device__ __forceinline__ void dm_load_io(const void *p, long idx, int io, float (&x)[CPL]) {
+__device__ __forceinline__ void dm_load_io(const void *p, size_t idx, int io, float (&x)[CPL]) {
   if (io == PACE_IO_F32) {
 #pragma unroll
     for (int e = 0; e < CPL; e += 2) {
@@ -143,68 +241,93 @@ __device__ __forceinline__ void dm_load_io(const void *p, long idx, int io, floa
 template <int CPL>
 __device__ __forceinline__ void dm_store_bytes(void *p, const int (&c)[CPL]) {
   if constexpr (CPL == 4)
-    *reinterpret_cast<uint32_t *>(p) = (uint32_t)(c[0] & 0xFF) | ((uint32_t)(c[1] & 0xFF) << 8) |
-                                       ((uint32_t)(c[2] & 0xFF) << 16) | ((uint32_t)(c[3] & 0xFF) << 24);
+    *reinterpret_cast<uint32_t *>(p) = __byte_perm(__byte_perm((uint32_t)c[0], (uint32_t)c[1], 0x0040),
+                                                   __byte_perm((uint32_t)c[2], (uint32_t)c[3], 0x0040), 0x5410);
   else
     *reinterpret_cast<uint16_t *>(p) = (uint16_t)((c[0] & 0xFF) | ((c[1] & 0xFF) << 8));
 }
 
-// Stage the buffered tokens and the new one (written into buffer slot m0) and compute the per-unit tables:
-// decay products, Gram coefficients W[t][s], readout coefficients cq / ck, group sums of every row.
+// The lane's packed words of column block cb: M-tiles 2cb, 2cb+1 (columns cb*32 + 16m + 8hi + lane/4), one
+// 16-byte vector per 64 keys and plane.
+template <int D, int PL>
+__device__ __forceinline__ void dm_load_block(const uint32_t *codes, int cb, int lane, uint32_t (&cw)[PL][2][D / 64][4]) {
+  constexpr int NPP = D / 64;
+#pragma unroll
+  for (int pl = 0; pl < PL; ++pl)
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int pp = 0; pp < NPP; ++pp) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(codes + pl * (D * D / 8) + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4);
+        cw[pl][m][pp][0] = v.x;
+        cw[pl][m][pp][1] = v.y;
+        cw[pl][m][pp][2] = v.z;
+        cw[pl][m][pp][3] = v.w;
+      }
+}
+
+// Stage the unit: its scales (and zero points), the buffered tokens and the new one (written into buffer
+// slot m0). Leaves in shared memory the key rows (then the q digits), the values, a_t, the key scales and
+// the digit weights (vsc), G_t and G_m/G_t. Returns beta_t and the value scale of token t = lane.
 template <int D, int G>
-__device__ void dm_stage(const PaceDev &st, const PaceIO &io, long unit, int m0, int has_token, const MmaShared &sh) {
+__device__ void dm_stage(const PaceDev &st, const PaceIO &io, int unit, int m0, int has_token, const MmaShared &sh,
+                         float &bt, float &sv_out) {
   constexpr int CPL = D / 32, NG = D / G;
   const int lane = threadIdx.x & 31;
   const int col0 = CPL * lane;
   const int dP = st.dP;
   const int mt = m0 + has_token;
-  const int nv = mt + (has_token ? 3 : 0);
   const int mixed = st.buf_mode == PACE_BUF_MIXED;
+  // asynchronous 16-byte copies, all in flight at once: scales, zero points, buffered rows (int8 keys
+  // straight into their rows, packed int4 keys of the mixed buffer into a scratch area first)
+  {
+    const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
+    for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(sh.ssc) + 16 * c, gs + 16 * c);
+    if (st.zero_point) {
+      const char *gz = reinterpret_cast<const char *>(st.zp + (size_t)unit * NG * D);
+      for (int c = lane; c < NG * D / 16; c += 32) cp_async16(sh.szp + 16 * c, gz + 16 * c);
+    }
+  }
+  const int rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
+  unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
+  if (m0 > 0) {
+    const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
+    const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
+    for (int c = lane; c < m0 * rk / 16; c += 32) cp_async16(kdst + 16 * c, gk + 16 * c);
+    for (int c = lane; c < m0 * rv / 16; c += 32) cp_async16(sh.vrow + 16 * c, gv + 16 * c);
+  }
   float sa = 0.0f, sb = 0.0f, ssk = 0.0f, ssv = 0.0f;
   if (lane < m0) {
     const float4 r = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
     sa = r.x; sb = r.y; ssk = r.z; ssv = r.w;
   }
-  for (int t = 0; t < m0; ++t) {
-    if (lane < D / 8) {                         // one 8-key run per lane, natural order
-      uint2 x;
-      if (mixed) {
-        const uint32_t nb = *reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(st.buf_k) +
-                                                                 ((size_t)unit * dP + t) * (D / 2) + 4 * lane);
+  float kx[CPL], vx[CPL], qx[CPL], an = 0.0f, bn = 0.0f;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) kx[c] = vx[c] = qx[c] = 0.0f;
+  if (has_token) {
+    dm_load_io<CPL>(io.k, (size_t)unit * D + col0, st.io, kx);
+    dm_load_io<CPL>(io.v, (size_t)unit * D + col0, st.io, vx);
+    dm_load_io<CPL>(io.q, (size_t)unit * D + col0, st.io, qx);
+    an = io.a[unit];
+    bn = io.beta[unit];
+  }
+  cp_async_wait_all();
+  __syncwarp();
+  if (mixed) {
+    for (int t = 0; t < m0; ++t) {
+      if (lane < D / 8) {                       // one 8-key run per lane: nibble code + 8 -> int8
+        const uint32_t nb = *reinterpret_cast<const uint32_t *>(kdst + t * (D / 2) + 4 * lane);
         uint32_t lo = 0, hi = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           lo |= (uint32_t)(((int)((nb >> (8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
           hi |= (uint32_t)(((int)((nb >> (16 + 8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
         }
-        x = make_uint2(lo, hi);
-      } else {
-        x = *reinterpret_cast<const uint2 *>(static_cast<const int8_t *>(st.buf_k) + ((size_t)unit * dP + t) * D + 8 * lane);
+        *reinterpret_cast<uint2 *>(sh.krow + t * D + 8 * lane) = make_uint2(lo, hi);
       }
-      *reinterpret_cast<uint2 *>(sh.krow + t * D + 8 * lane) = x;
-    }
-    if (mixed) {
-      const uint32_t *src = reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(st.buf_v) +
-                                                               ((size_t)unit * dP + t) * D + col0);
-      uint32_t *dst = reinterpret_cast<uint32_t *>(sh.vrow + ((size_t)t * D + col0) * 2);
-#pragma unroll
-      for (int e = 0; e < CPL / 2; ++e) dst[e] = src[e];
-    } else {
-      const int8_t *src = static_cast<const int8_t *>(st.buf_v) + ((size_t)unit * dP + t) * D + col0;
-      if constexpr (CPL == 4)
-        *reinterpret_cast<uint32_t *>(sh.vrow + t * D + col0) = *reinterpret_cast<const uint32_t *>(src);
-      else
-        *reinterpret_cast<uint16_t *>(sh.vrow + t * D + col0) = *reinterpret_cast<const uint16_t *>(src);
     }
   }
-  float qx[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) qx[c] = 0.0f;
   if (has_token) {
-    float kx[CPL], vx[CPL];
-    dm_load_io<CPL>(io.k, unit * D + col0, st.io, kx);
-    dm_load_io<CPL>(io.v, unit * D + col0, st.io, vx);
-    dm_load_io<CPL>(io.q, unit * D + col0, st.io, qx);
     float mk = 0.0f, mv = 0.0f, mq = 0.0f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
@@ -213,11 +336,14 @@ __device__ void dm_stage(const PaceDev &st, const PaceIO &io, long unit, int m0,
       mq = fmaxf(mq, fabsf(qx[c]));
     }
     const float Ak = warp_max(mk), Av = warp_max(mv), Aq = warp_max(mq);
+    // per-token buffer quantizer: s = A/qmax, code = clamp(rint(x * fl(qmax/A))), zero codes for A = 0
     const int qk = mixed ? 7 : 127;
-    const float sk = buffer_scale(Ak, qk);
+    const bool kz = !(Ak >= FLT_MIN);
+    const float rkk = kz ? 0.0f : __fdiv_rn((float)qk, Ak);
+    const float sk = kz ? 0.0f : __fdiv_rn(Ak, (float)qk);
     int ck[CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) ck[c] = buffer_code(kx[c], Ak, qk);
+    for (int c = 0; c < CPL; ++c) ck[c] = min(max(__float2int_rn(__fmul_rn(kx[c], rkk)), -qk), qk);
     dm_store_bytes<CPL>(sh.krow + m0 * D + col0, ck);
     float sv = 0.0f;
     if (mixed) {
@@ -233,15 +359,16 @@ __device__ void dm_stage(const PaceDev &st, const PaceIO &io, long unit, int m0,
         vr[c / 2] = *reinterpret_cast<const uint32_t *>(&pv);
       }
     } else {
-      sv = buffer_scale(Av, 127);
+      const bool vz = !(Av >= FLT_MIN);
+      const float rvv = vz ? 0.0f : __fdiv_rn(127.0f, Av);
+      sv = vz ? 0.0f : __fdiv_rn(Av, 127.0f);
       int cv[CPL];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) cv[c] = buffer_code(vx[c], Av, 127);
+      for (int c = 0; c < CPL; ++c) cv[c] = min(max(__float2int_rn(__fmul_rn(vx[c], rvv)), -127), 127);
       dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * D + col0, ck);
       dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0, cv);
       dm_store_bytes<CPL>(sh.vrow + m0 * D + col0, cv);
     }
-    const float an = io.a[unit], bn = io.beta[unit];
     if (lane == m0) {
       sa = an; sb = bn; ssk = sk; ssv = sv;
     }
@@ -249,12 +376,13 @@ __device__ void dm_stage(const PaceDev &st, const PaceIO &io, long unit, int m0,
       *reinterpret_cast<float4 *>(st.buf_s + ((size_t)unit * dP + m0) * 4) = make_float4(an, bn, sk, sv);
     // q ~= sigma (65536 d2 + 256 d1 + d0), |qi| <= 127 * 65536, balanced base-256 digits in [-128, 127]
     const float QMAX = 8323072.0f;
-    const float sigma = Aq >= FLT_MIN ? Aq / QMAX : 0.0f;
+    const bool qz = !(Aq >= FLT_MIN);
+    const float sigma = qz ? 0.0f : __fdiv_rn(Aq, QMAX);
+    const float rq = qz ? 0.0f : __fdiv_rn(QMAX, Aq);
     int d2[CPL], d1[CPL], d0[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-      int qi = 0;
-      if (Aq >= FLT_MIN) qi = min(max(__float2int_rn(qx[c] * (QMAX / Aq)), -8323072), 8323072);
+      const int qi = min(max(__float2int_rn(qx[c] * rq), -8323072), 8323072);
       const int q1 = (qi + 128) >> 8;
       d0[c] = qi - (q1 << 8);
       d2[c] = (q1 + 128) >> 8;
@@ -272,83 +400,96 @@ __device__ void dm_stage(const PaceDev &st, const PaceIO &io, long unit, int m0,
   if (lane < mt) {
     sh.a[lane] = sa;
     sh.vsc[lane] = ssk;
-    sh.bt[lane] = sb;
-    sh.sv[lane] = ssv;
   }
+  bt = sb;
+  sv_out = ssv;
   __syncwarp();
-  // group sums of every staged row
-  for (int p = lane; p < nv * NG; p += 32) {
-    const int v = p / NG, g = p - v * NG;
-    int s = 0;
-#pragma unroll
-    for (int i4 = 0; i4 < G / 4; ++i4) s = dp4a_ss(*reinterpret_cast<const int *>(sh.krow + v * D + g * G + 4 * i4), 0x01010101, s);
-    sh.csum[v * 4 + g] = s;
-  }
-  // decay products, Gram coefficients, readout coefficients
   if (lane < mt) {
+    const int ws = dm_wstride(dP);
     float g = 1.0f, dm = 1.0f;
     for (int r = 0; r <= lane; ++r) g *= sh.a[r];
     for (int r = lane + 1; r < mt; ++r) dm *= sh.a[r];
     sh.gam[lane] = g;
     sh.dmq[lane] = dm;
-  }
-  const int npairs = mt * (mt - 1) / 2;
-  for (int p = lane; p < npairs; p += 32) {
-    int t = 1, base = 0;
-    while (base + t <= p) {
-      base += t;
-      ++t;
-    }
-    const int s = p - base;
-    float dm = 1.0f;
-    for (int r = s + 1; r <= t; ++r) dm *= sh.a[r];
-    int dot = 0;
-#pragma unroll
-    for (int i4 = 0; i4 < D / 4; ++i4)
-      dot = dp4a_ss(*reinterpret_cast<const int *>(sh.krow + s * D + 4 * i4),
-                    *reinterpret_cast<const int *>(sh.krow + t * D + 4 * i4), dot);
-    sh.W[t * dP + s] = dm * sh.vsc[s] * sh.vsc[t] * (float)dot;
-  }
-  __syncwarp();
-  for (int s = 0; s < mt; ++s) {
-    float part = 0.0f;
-    if (has_token) {
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) part += (float)sh.krow[s * D + col0 + c] * qx[c];
-      part = warp_sum(part);
-    }
-    if (lane == 0) {
-      const float dv = sh.dmq[s] * sh.vsc[s];
-      sh.cq[s] = dv * part;
-      sh.ck[s] = dv;
+    float p = 1.0f;                             // G_t/G_s = a_{s+1} .. a_t for t = lane, s < t
+    for (int s = lane - 1; s >= 0; --s) {
+      p *= sh.a[s + 1];
+      sh.dmt[lane * ws + s] = p;
     }
   }
-  __syncwarp();
 }
 
-// The MMA operand tables: A fragments of the staged vectors for the dots (rows >= nv are zero) and, for
-// a flush, the bf16 key table kbf[i][s] (s >= mt zero).
-template <int D>
-__device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dpp, int do_flush) {
-  constexpr int KS = D / 16;
+// Unit tables: the fp16 rows of the staged vectors (rows >= nv zero; keys 8..15 of every 16-key step
+// scaled by 1/16); then, by MMAs of those rows, the group sums (T1, T2), the Gram coefficients W and the
+// digit products k_s.q; the per-token replay table; for a flush the bf16 key table kbf[i][s].
+template <int D, int G>
+__device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, int has_token, int do_flush,
+                          float bt, float sv) {
+  constexpr int KS = D / 16, KSG = G / 16, NG = D / G;
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int nvt = (nv + 15) >> 4;
+  const int ws = dm_wstride(dP);
+  for (int idx = lane; idx < 16 * nvt * (D / 8); idx += 32) {   // 8 keys per item
+    const int row = idx / (D / 8), k8 = 8 * (idx - row * (D / 8));
+    uint4 h = make_uint4(0u, 0u, 0u, 0u);
+    if (row < nv) {
+      const uint2 x = *reinterpret_cast<const uint2 *>(sh.krow + row * D + k8);
+      const bool sx = (k8 & 8) != 0;
+      h = make_uint4(i8pair_f16(x.x, 0x4140, sx), i8pair_f16(x.x, 0x4342, sx), i8pair_f16(x.y, 0x4140, sx),
+                     i8pair_f16(x.y, 0x4342, sx));
+    }
+    *reinterpret_cast<uint4 *>(sh.ah + ah_off<D>(row, k8 >> 3)) = h;
+  }
+  __syncwarp();
+  const int ntg = (mt + 7) >> 3;                 // 8-token tiles of the Gram columns
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;   // ldmatrix x4: row, chunk
+  const int brow = lane & 7, bcol = (lane >> 3) & 1;                       // ldmatrix x2: row, chunk
   for (int vt = 0; vt < nvt; ++vt) {
-#pragma unroll 4
+    float cs[4], gr[4][4];
+#pragma unroll 2
     for (int ks = 0; ks < KS; ++ks) {
-      const int k0 = 16 * ks + 2 * tq;
-      uint32_t w[4];
+      uint32_t a[4];
+      ldsm_x4(a, sh.ah + ah_off<D>(16 * vt + arow, 2 * ks + acol));
+      const int gi = ks / KSG;                   // sums: column 2gi (first halves), 2gi + 1 (second halves)
+      const uint32_t o0 = g8 == 2 * gi ? 0x3C003C00u : 0u, o1 = g8 == 2 * gi + 1 ? 0x3C003C00u : 0u;
+      if (ks == 0) mma_f16_z(cs, a, o0, o1); else mma_f16(cs, a, o0, o1);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = 16 * vt + g8 + 8 * (q & 1), key = k0 + 8 * (q >> 1);
-        w[q] = 0u;
-        if (row < nv) {
-          const int8_t *p = sh.krow + row * D + key;
-          w[q] = bf16x2_bits((float)p[0], (float)p[1]);
+      for (int n = 0; n < 4; ++n) {
+        if (n < ntg) {
+          uint32_t bb[2];
+          ldsm_x2(bb, sh.ah + ah_off<D>(8 * n + brow, 2 * ks + bcol));
+          const uint32_t b1 = f16x2_scale(bb[1], 256.0f);
+          if (ks == 0) mma_f16_z(gr[n], a, bb[0], b1); else mma_f16(gr[n], a, bb[0], b1);
         }
       }
-      sh.abf[(vt * KS + ks) * 32 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    const int v0 = 16 * vt + g8;
+    if (tq < NG) {
+      sh.cf[v0 * 4 + tq] = make_float2(1024.0f * (cs[0] + cs[1]), cs[0] + 16.0f * cs[1]);
+      sh.cf[(v0 + 8) * 4 + tq] = make_float2(1024.0f * (cs[2] + cs[3]), cs[2] + 16.0f * cs[3]);
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      if (n >= ntg) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = v0 + 8 * (e >> 1), s = 8 * n + 2 * tq + (e & 1);
+        if (s >= mt) continue;
+        if (v < mt && s < v)
+          sh.W[v * ws + s] = sh.dmt[v * ws + s] * sh.vsc[s] * sh.vsc[v] * gr[n][e];
+        else if (v >= mt && v < nv)
+          sh.e3[(v - mt) * dP + s] = gr[n][e];
+      }
+    }
+  }
+  __syncwarp();
+  if (lane < mt) {
+    const float dv = sh.dmq[lane] * sh.vsc[lane];
+    const float cq = has_token ? dv * (sh.vsc[mt] * sh.e3[lane] + (sh.vsc[mt + 1] * sh.e3[dP + lane] +
+                                                                   sh.vsc[mt + 2] * sh.e3[2 * dP + lane]))
+                               : 0.0f;
+    sh.ck[lane] = dv;
+    sh.tk[lane] = make_float4(sh.gam[lane] * sh.vsc[lane], bt, sv, cq);
   }
   if (do_flush) {
     const int half = dpp >> 1;
@@ -362,70 +503,16 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dpp, int do_f
   __syncwarp();
 }
 
-// Requantize one key-axis group of one column from the lane quad that holds it (NV values per lane, the
-// quad together holding the group), with the arithmetic of quant_group. Returns the stored codes.
-template <int NV, int BITS>
-__device__ __forceinline__ void quad_quant(const float (&x)[NV], int zero_point, uint32_t (&u)[NV], float &s_out,
-                                           int &z_out) {
-  float s;
-  int z;
-  if (!zero_point) {
-    constexpr int qmax = (1 << (BITS - 1)) - 1;
-    float A = 0.0f;
-#pragma unroll
-    for (int e = 0; e < NV; ++e) A = fmaxf(A, fabsf(x[e]));
-    A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 1));
-    A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 2));
-    s = bf16_round(__fdiv_rn(A, (float)qmax));
-    z = 1 << (BITS - 1);
-    if (!(s >= FLT_MIN)) s = 0.0f;
-  } else {
-    constexpr int qm = (1 << BITS) - 1;
-    float lo = 0.0f, hi = 0.0f;
-#pragma unroll
-    for (int e = 0; e < NV; ++e) {
-      lo = fminf(lo, x[e]);
-      hi = fmaxf(hi, x[e]);
-    }
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
-    s = bf16_round(__fdiv_rn(__fsub_rn(hi, lo), (float)qm));
-    z = 0;
-    if (!(s >= FLT_MIN))
-      s = 0.0f;
-    else
-      z = min(max(__float2int_rn(__fmul_rn(-lo, __fdiv_rn(1.0f, s))), 0), qm);
-  }
-  const float r = s > 0.0f ? __fdiv_rn(1.0f, s) : 0.0f;
-#pragma unroll
-  for (int e = 0; e < NV; ++e) {
-    int c;
-    if (s == 0.0f) {
-      c = z;
-    } else if (!zero_point) {
-      constexpr int qmax = (1 << (BITS - 1)) - 1;
-      c = min(max(__float2int_rn(__fmul_rn(x[e], r)), -qmax), qmax) + z;
-    } else {
-      constexpr int qm = (1 << BITS) - 1;
-      c = min(max(__float2int_rn(__fmul_rn(x[e], r)) + z, 0), qm);
-    }
-    u[e] = (uint32_t)c;
-  }
-  s_out = s;
-  z_out = z;
-}
-
 template <int D, int G, int BITS>
-__device__ void dm_unit(const PaceDev &st, const PaceIO &io, long unit, int m0, int has_token, const MmaShared &sh) {
-  constexpr int NG = D / G, NPP = D / 64, KS = D / 16, KSG = G / 16, PL = BITS / 4;
+__device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int m0, int has_token,
+                        const MmaShared &sh) {
+  constexpr int NG = D / G, NPP = D / 64, KSG = G / 16, PL = BITS / 4;
   constexpr int NKG = G / 8;            // key n-tiles (8 keys) per group
   constexpr int NH = BITS == 8 ? 2 : 1, NPN = 4 / NH;   // dot passes, column n-tiles per pass
   constexpr uint32_t PLANE = D * D / 8; // words per nibble plane
+  constexpr int OFF = 1 << (BITS - 1);  // symmetric code offset
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int dP = st.dP;
-  const int b = (int)(unit / st.H), h = (int)(unit - (long)b * st.H);
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
   const int nv = mt + (has_token ? 3 : 0);
@@ -433,50 +520,31 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, long unit, int m0, 
   const int dpp = dm_dpp(dP);
   const int mixed = st.buf_mode == PACE_BUF_MIXED;
   const int zpm = st.zero_point;
-  uint32_t *codes = dm_unit_codes<D, BITS>(st, b, h);
+  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
+                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
   __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
   uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
 
-  if (lane == 0) {                       // the unit's resident bytes start moving into L2 right away
-    prefetch_l2(codes, PL * PLANE * 4);
-    prefetch_l2(scale, NG * D * 2);
-    if (zpm) prefetch_l2(zpt, NG * D);
-    if (m0 > 0) {
-      const uint32_t rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
-      prefetch_l2(static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk, m0 * rk);
-      prefetch_l2(static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv, m0 * rv);
-    }
-  }
-  dm_stage<D, G>(st, io, unit, m0, has_token, sh);
-  dm_tables<D>(sh, nv, mt, dpp, do_flush);
+  if (lane == 0) prefetch_l2(codes, PL * PLANE * 4);   // the unit's code words start moving right away
+  // the lane's packed words of the first column block load while the buffer is staged
+  uint32_t cw[PL][2][NPP][4];
+  dm_load_block<D, PL>(codes, 0, lane, cw);
+  float bt, sv;
+  dm_stage<D, G>(st, io, unit, m0, has_token, sh, bt, sv);
+  dm_tables<D, G>(sh, nv, mt, dP, dpp, has_token, do_flush, bt, sv);
   const float gm = sh.gam[mt - 1];
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;
 
 #pragma unroll 1
   for (int cb = 0; cb < D / 32; ++cb) {
-    // ---- the lane's packed words of this block: M-tiles 2cb, 2cb+1 (columns cb*32 + 16m + 8hi + g8)
-    uint32_t cw[PL][2][NPP][4];
-#pragma unroll
-    for (int pl = 0; pl < PL; ++pl)
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int pp = 0; pp < NPP; ++pp) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(codes + pl * PLANE + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4);
-          cw[pl][m][pp][0] = v.x;
-          cw[pl][m][pp][1] = v.y;
-          cw[pl][m][pp][2] = v.z;
-          cw[pl][m][pp][3] = v.w;
-        }
+    if (cb > 0 && do_flush) dm_load_block<D, PL>(codes, cb, lane, cw);
 
     // ---- dots: P[v][j] for the 32 columns of the block; n-tile n = columns cb*32 + 8n .. +7
 #pragma unroll 1
     for (int vt = 0; vt < nvt; ++vt) {
       const int v0 = 16 * vt + g8;
+      const int ar = 16 * vt + arow;
       float pacc[4][4];
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pacc[n][e] = 0.0f;
 #pragma unroll
       for (int nh = 0; nh < NH; ++nh)          // int8 heads: two passes of two n-tiles (register budget)
 #pragma unroll
@@ -485,50 +553,50 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, long unit, int m0, 
 #pragma unroll
           for (int q = 0; q < NPN; ++q) {
             const int j = cb * 32 + 8 * (nh * NPN + q) + 2 * tq;
-            sc[q] = *reinterpret_cast<const uint32_t *>(scale + gi * D + j);
-            zz[q] = zpm ? (uint32_t)*reinterpret_cast<const uint16_t *>(zpt + gi * D + j) : 0u;
+            sc[q] = *reinterpret_cast<const uint32_t *>(sh.ssc + gi * D + j);
+            zz[q] = zpm ? (uint32_t)*reinterpret_cast<const uint16_t *>(sh.szp + gi * D + j) : 0u;
           }
           float dacc[PL][NPN][4];
 #pragma unroll
-          for (int pl = 0; pl < PL; ++pl)
-#pragma unroll
-            for (int q = 0; q < NPN; ++q)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) dacc[pl][q][e] = 0.0f;
-#pragma unroll
           for (int kk = 0; kk < KSG; ++kk) {
             const int ks = gi * KSG + kk;
-            const uint4 av = sh.abf[(vt * KS + ks) * 32 + lane];
-            const uint32_t a[4] = {av.x, av.y, av.z, av.w};
-            const int r = 2 * (ks & 1);
+            uint32_t a[4];
+            ldsm_x4(a, sh.ah + ah_off<D>(ar, 2 * ks + acol));
 #pragma unroll
             for (int q = 0; q < NPN; ++q)
 #pragma unroll
               for (int pl = 0; pl < PL; ++pl) {
                 const int n = nh * NPN + q;
-                const uint32_t w = cw[pl][n >> 1][ks >> 2][(n & 1) * 2 + ((ks >> 1) & 1)];
-                mma16(dacc[pl][q], a, nib_pair(w, r), nib_pair(w, r + 1));
+                uint32_t w = cw[pl][n >> 1][ks >> 2][(n & 1) * 2 + ((ks >> 1) & 1)];
+                if (ks & 1) w >>= 8;
+                const uint32_t b0 = (w & 0x000F000Fu) | 0x64006400u, b1 = (w & 0x00F000F0u) | 0x64006400u;
+                if (kk == 0) mma_f16_z(dacc[pl][q], a, b0, b1); else mma_f16(dacc[pl][q], a, b0, b1);
               }
           }
-          // fold the group: P += s_gj sum_i (u_ij - z_gj) B[v][i]
-          const int cs0 = v0 < nv ? sh.csum[v0 * 4 + gi] : 0;
-          const int cs1 = v0 + 8 < nv ? sh.csum[(v0 + 8) * 4 + gi] : 0;
+          // fold the group: P += s_gj (D - T1 - z_gj T2)
+          const float2 c0 = sh.cf[v0 * 4 + gi], c1 = sh.cf[(v0 + 8) * 4 + gi];
+          const float k0 = fmaf((float)OFF, c0.y, c0.x), k1 = fmaf((float)OFF, c1.y, c1.x);
 #pragma unroll
-          for (int q = 0; q < NPN; ++q)
+          for (int q = 0; q < NPN; ++q) {
+            const int n = nh * NPN + q;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int n = nh * NPN + q;
               const float s = (e & 1) ? bf16_hi(sc[q]) : bf16_lo(sc[q]);
-              const int zj = zpm ? (int)((zz[q] >> (8 * (e & 1))) & 0xFFu) : (1 << (BITS - 1));
-              const int cs = (e >> 1) ? cs1 : cs0;
+              const float2 c = (e >> 1) ? c1 : c0;
               float tot;
               if (BITS == 4) {
-                tot = fmaf(-(float)(128 + zj), (float)cs, dacc[0][q][e]);
+                if (!zpm)
+                  tot = dacc[0][q][e] - ((e >> 1) ? k1 : k0);
+                else
+                  tot = dacc[0][q][e] - fmaf((float)((zz[q] >> (8 * (e & 1))) & 0xFFu), c.y, c.x);
               } else {
-                tot = (float)(__float2int_rn(dacc[0][q][e]) + 16 * __float2int_rn(dacc[PL - 1][q][e]) - (2176 + zj) * cs);
+                const int zj = zpm ? (int)((zz[q] >> (8 * (e & 1))) & 0xFFu) : OFF;
+                tot = (float)(__float2int_rn(dacc[0][q][e]) + 16 * __float2int_rn(dacc[PL - 1][q][e]) -
+                              17 * __float2int_rn(c.x) - zj * __float2int_rn(c.y));
               }
               pacc[n][e] = gi == 0 ? s * tot : fmaf(s, tot, pacc[n][e]);
             }
+          }
         }
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
@@ -537,67 +605,67 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, long unit, int m0, 
           *reinterpret_cast<float2 *>(sh.pb + (v0 + 8) * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][2], pacc[n][3]);
       }
     }
+    // without a flush the block's words are done with: the next block's load overlaps the replay
+    if (!do_flush && cb + 1 < D / 32) dm_load_block<D, PL>(codes, cb + 1, lane, cw);
     __syncwarp();
 
     // ---- replay and readout: lane = column cb*32 + lane
     {
       const int j = cb * 32 + lane;
-      for (int t = 0; t < mt; ++t) {
-        float vt;
-        if (mixed)
-          vt = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(sh.vrow)[t * D + j]);
-        else
-          vt = sh.sv[t] * (float)reinterpret_cast<const int8_t *>(sh.vrow)[t * D + j];
-        float acc = vt - sh.gam[t] * (sh.vsc[t] * sh.pb[t * PB_STRIDE + lane]);
-        for (int s = 0; s < t; ++s) acc = fmaf(-sh.W[t * dP + s], sh.ub[s * UB_STRIDE + lane], acc);
-        sh.ub[t * UB_STRIDE + lane] = sh.bt[t] * acc;
+      auto value = [&](int t, float svt) -> float {
+        if (mixed) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(sh.vrow)[t * D + j]);
+        return svt * (float)reinterpret_cast<const int8_t *>(sh.vrow)[t * D + j];
+      };
+      float o = 0.0f;
+      if (has_token)
+        o = gm * (sh.vsc[mt] * sh.pb[mt * PB_STRIDE + lane] +
+                  (sh.vsc[mt + 1] * sh.pb[(mt + 1) * PB_STRIDE + lane] + sh.vsc[mt + 2] * sh.pb[(mt + 2) * PB_STRIDE + lane]));
+      if (dP <= 8) {                           // u in registers
+        float u[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          u[t] = 0.0f;
+          if (t < mt) {
+            const float4 tk = sh.tk[t];          // G_t s_kt, beta_t, s_vt, readout coefficient
+            float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
+#pragma unroll
+            for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * 8 + s2], u[s2], acc);
+            u[t] = tk.y * acc;
+            o = fmaf(tk.w, u[t], o);
+            if (do_flush) sh.ub[t * UB_STRIDE + lane] = u[t];
+          }
+        }
+      } else {
+        for (int t = 0; t < mt; ++t) {
+          const float4 tk = sh.tk[t];
+          float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
+          for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * dP + s2], sh.ub[s2 * UB_STRIDE + lane], acc);
+          const float ut = tk.y * acc;
+          sh.ub[t * UB_STRIDE + lane] = ut;
+          o = fmaf(tk.w, ut, o);
+        }
       }
-      if (has_token) {
-        float o = gm * (sh.vsc[mt] * sh.pb[mt * PB_STRIDE + lane] +
-                        (sh.vsc[mt + 1] * sh.pb[(mt + 1) * PB_STRIDE + lane] + sh.vsc[mt + 2] * sh.pb[(mt + 2) * PB_STRIDE + lane]));
-        for (int s = 0; s < mt; ++s) o = fmaf(sh.cq[s], sh.ub[s * UB_STRIDE + lane], o);
-        store_io(io.o, unit * D + j, o, st.io);
-      }
+      if (has_token) store_io(io.o, (long)unit * D + j, o, st.io);
     }
     __syncwarp();
     if (!do_flush) continue;
 
-    // ---- flush: rebuild and requantize the block's columns, M-tile by M-tile
+    // ---- flush: rebuild and requantize the block's columns, M-tile by M-tile, group by group
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const int jl = 16 * m + g8;              // local columns jl (hi = 0) and jl + 8 (hi = 1)
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
-        float fs[2];
-        int fz[2];
+        float fs[2], fz[2];
 #pragma unroll
         for (int hi = 0; hi < 2; ++hi) {
           const int j = cb * 32 + jl + 8 * hi;
-          fs[hi] = gm * __bfloat162float(scale[gi * D + j]);
-          fz[hi] = zpm ? (int)zpt[gi * D + j] : (1 << (BITS - 1));
+          fs[hi] = gm * __bfloat162float(sh.ssc[gi * D + j]);
+          fz[hi] = -(8388608.0f + (float)(zpm ? (int)sh.szp[gi * D + j] : OFF));
         }
-        __syncwarp();                          // the quad has read the old scale before lane 0 replaces it
         float c[NKG][4];
-#pragma unroll
-        for (int nn = 0; nn < NKG; ++nn) {
-          const int nk = gi * NKG + nn;
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int wi = hi * 2 + ((nk >> 2) & 1), r = nk & 3;
-            uint32_t u0 = (cw[0][m][nk >> 3][wi] >> (4 * r)) & 0xFu;
-            uint32_t u1 = (cw[0][m][nk >> 3][wi] >> (16 + 4 * r)) & 0xFu;
-            if (BITS == 8) {
-              u0 |= ((cw[PL - 1][m][nk >> 3][wi] >> (4 * r)) & 0xFu) << 4;
-              u1 |= ((cw[PL - 1][m][nk >> 3][wi] >> (16 + 4 * r)) & 0xFu) << 4;
-            }
-            c[nn][2 * hi] = fs[hi] * (float)((int)u0 - fz[hi]);
-            c[nn][2 * hi + 1] = fs[hi] * (float)((int)u1 - fz[hi]);
-          }
-        }
-#pragma unroll 1
-        for (int sb = 0; sb < (dpp >> 3); ++sb) {
-          // A: the three bf16 parts of rho_s u_s,j for tokens s = 8sb + 2tq, +1 and columns jl, jl + 8
-          uint32_t ap[3][2];
+        // A: the three bf16 parts of rho_s u_s,j for tokens s = 8sb + 2tq, +1 and columns jl, jl + 8
+        auto parts = [&](int sb, uint32_t (&ap)[3][2]) {
 #pragma unroll
           for (int hi = 0; hi < 2; ++hi) {
             const int s0 = 8 * sb + 2 * tq;
@@ -606,50 +674,114 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, long unit, int m0, 
             const uint32_t p0 = bf16x2_bits(x0, x1);
             const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
             const uint32_t p1 = bf16x2_bits(r0, r1);
-            const uint32_t p2 = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
             ap[0][hi] = p0;
             ap[1][hi] = p1;
-            ap[2][hi] = p2;
+            ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
           }
+        };
+        {
+          uint32_t ap[3][2];
+          parts(0, ap);
           const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
 #pragma unroll
           for (int nn = 0; nn < NKG; ++nn) {
-            const int i = 8 * (gi * NKG + nn) + g8;
-            const uint32_t bk = sh.kbf[i * (dpp >> 1) + 4 * sb + tq];
-            mma16(c[nn], a16, bk, bk);
-            mma8(c[nn], ap[2][0], ap[2][1], bk);
+            const uint32_t bk = sh.kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + tq];
+            mma_bf16_z(c[nn], a16, bk, bk);
+            mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
+          }
+        }
+#pragma unroll 1
+        for (int sb = 1; sb < (dpp >> 3); ++sb) {
+          uint32_t ap[3][2];
+          parts(sb, ap);
+          const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
+#pragma unroll
+          for (int nn = 0; nn < NKG; ++nn) {
+            const uint32_t bk = sh.kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + 4 * sb + tq];
+            mma_bf16(c[nn], a16, bk, bk);
+            mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
+          }
+        }
+        // the old state: x = G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
+#pragma unroll
+        for (int nn = 0; nn < NKG; ++nn) {
+          const int nk = gi * NKG + nn, r = nk & 3;
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int wi = hi * 2 + ((nk >> 2) & 1);
+            uint32_t m16 = (cw[0][m][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu;
+            if (BITS == 8) m16 |= ((cw[PL - 1][m][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu) << 4;
+            const float2 f = make_float2(__uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7610)),
+                                         __uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7632)));
+            const float2 d = __fadd2_rn(f, make_float2(fz[hi], fz[hi]));
+            const float2 x = __ffma2_rn(make_float2(fs[hi], fs[hi]), d, make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]));
+            c[nn][2 * hi] = x.x;
+            c[nn][2 * hi + 1] = x.y;
           }
         }
         // requantize the group for both columns; the lane's keys fill its own words
 #pragma unroll
         for (int hi = 0; hi < 2; ++hi) {
-          float x[2 * NKG];
+          float s;
+          int z;
+          if (!zpm) {
+            float A = 0.0f;
 #pragma unroll
-          for (int nn = 0; nn < NKG; ++nn) {
-            x[2 * nn] = c[nn][2 * hi];
-            x[2 * nn + 1] = c[nn][2 * hi + 1];
+            for (int nn = 0; nn < NKG; ++nn) A = fmax3(A, fabsf(c[nn][2 * hi]), fabsf(c[nn][2 * hi + 1]));
+            A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 1));
+            A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 2));
+            constexpr float QMAX = (float)(OFF - 1);
+            s = bf16_quot(A, QMAX, 1.0f / QMAX);
+            z = OFF;
+          } else {
+            float lo = 0.0f, hi_ = 0.0f;
+#pragma unroll
+            for (int nn = 0; nn < NKG; ++nn) {
+              lo = fmin3(lo, c[nn][2 * hi], c[nn][2 * hi + 1]);
+              hi_ = fmax3(hi_, c[nn][2 * hi], c[nn][2 * hi + 1]);
+            }
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+            hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 1));
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
+            hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 2));
+            constexpr float QM = (float)((1 << BITS) - 1);
+            s = bf16_quot(__fsub_rn(hi_, lo), QM, 1.0f / QM);
+            z = 0;
+            if (s >= FLT_MIN) z = min(max(__float2int_rn(__fmul_rn(-lo, rcp_bf16(s))), 0), (1 << BITS) - 1);
           }
-          uint32_t u[2 * NKG];
-          float s_new;
-          int z_new;
-          quad_quant<2 * NKG, BITS>(x, zpm, u, s_new, z_new);
+          if (!(s >= FLT_MIN)) s = 0.0f;
+          const float r = s > 0.0f ? rcp_bf16(s) : 0.0f;
+          // codes: rint(x r) by the 1.5 * 2^23 rounding constant (symmetric: the clamp to +-qmax never binds,
+          // since s = bf16(A / qmax) puts |x r| below qmax + 1/2); zero point: + z, clamp to [0, 2^b - 1]
+          const float2 r2 = make_float2(r, r);
+          const float mg = zpm ? 12582912.0f : 12582912.0f + (float)OFF;
+          const float2 mg2 = make_float2(mg, mg);
 #pragma unroll
           for (int pw = 0; pw < G / 32; ++pw) {
             const int p = gi * (G / 32) + pw;  // 32-key span
-            uint32_t lo = 0, hw = 0;
+            uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int nn = 4 * pw + r;
-              lo |= ((u[2 * nn] & 0xFu) << (4 * r)) | ((u[2 * nn + 1] & 0xFu) << (16 + 4 * r));
-              hw |= (((u[2 * nn] >> 4) & 0xFu) << (4 * r)) | (((u[2 * nn + 1] >> 4) & 0xFu) << (16 + 4 * r));
+            for (int rr = 0; rr < 4; ++rr) {
+              const int nn = 4 * pw + rr;
+              const float2 y = __fadd2_rn(__fmul2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2), mg2);
+              uint32_t pair;
+              if (!zpm) {
+                pair = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410) & 0x00FF00FFu;
+              } else {
+                const int c0 = min(max((int)(__float_as_uint(y.x) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
+                const int c1 = min(max((int)(__float_as_uint(y.y) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
+                pair = __byte_perm((uint32_t)c0, (uint32_t)c1, 0x5410);
+              }
+              w0 += (pair & 0x000F000Fu) << (4 * rr);
+              if (BITS == 8) w1 += ((pair >> 4) & 0x000F000Fu) << (4 * rr);
             }
-            cw[0][m][p >> 1][hi * 2 + (p & 1)] = lo;
-            if (BITS == 8) cw[PL - 1][m][p >> 1][hi * 2 + (p & 1)] = hw;
+            cw[0][m][p >> 1][hi * 2 + (p & 1)] = w0;
+            if (BITS == 8) cw[PL - 1][m][p >> 1][hi * 2 + (p & 1)] = w1;
           }
           if (tq == 0) {
             const int j = cb * 32 + jl + 8 * hi;
-            scale[gi * D + j] = __float2bfloat16_rn(s_new);
-            if (zpm) zpt[gi * D + j] = (uint8_t)z_new;
+            scale[gi * D + j] = __float2bfloat16_rn(s);
+            if (zpm) zpt[gi * D + j] = (uint8_t)z;
           }
         }
       }
@@ -672,22 +804,22 @@ template <int D, int G, int BITS>
 __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const MmaSmem L = mma_smem(D, st.dP, st.buf_mode == PACE_BUF_MIXED);
-  const MmaShared sh = mma_shared(smem + (size_t)warp * L.total, L);
   const int HP = BITS == 4 ? st.H4 : st.H8;
-  const long w = (long)blockIdx.x * DM_WARPS + warp;
-  if (w >= (long)st.B * HP) return;
-  const int b = (int)(w / HP), slot = (int)(w - (long)b * HP);
+  const int w = blockIdx.x * DM_WARPS + warp;
+  if (w >= st.B * HP) return;
+  const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
-  const long u = (long)b * st.H + h;
+  const int u = b * st.H + h;
   const int m0 = st.m[u];
   if (m0 < 0 || m0 >= st.dP) {                  // corrupted counter: leave the unit, emit zeros
     if (has_token)
-      for (int c = lane; c < D; c += 32) store_io(io.o, u * D + c, 0.0f, st.io);
+      for (int c = lane; c < D; c += 32) store_io(io.o, (long)u * D + c, 0.0f, st.io);
     return;
   }
   if (!has_token && m0 == 0) return;            // flush with nothing pending
-  dm_unit<D, G, BITS>(st, io, u, m0, has_token, sh);
+  const MmaSmem L = mma_smem(D, G, st.dP, st.buf_mode == PACE_BUF_MIXED, st.zero_point);
+  const MmaShared sh = mma_shared(smem + (size_t)warp * L.total, L, st.dP);
+  dm_unit<D, G, BITS>(st, io, b, h, u, m0, has_token, sh);
   __syncwarp();
   if (lane == 0) st.m[u] = (!has_token || m0 + 1 == st.dP) ? 0 : m0 + 1;
 }
@@ -710,7 +842,7 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
 
 template <int D, int G>
 static cudaError_t launch_mma_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  const MmaSmem L = mma_smem(D, d.dP, d.buf_mode == PACE_BUF_MIXED);
+  const MmaSmem L = mma_smem(D, G, d.dP, d.buf_mode == PACE_BUF_MIXED, d.zero_point);
   const size_t smem = (size_t)DM_WARPS * L.total;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = launch_pool<D, G, 4>(d, io, has_token, s, smem);
