@@ -266,28 +266,51 @@ __device__ __forceinline__ void dm_load_block(const uint32_t *codes, int cb, int
       }
 }
 
-// Stage the unit: its scales (and zero points), the buffered tokens and the new one (written into buffer
-// slot m0). Leaves in shared memory the key rows (then the q digits), the values, a_t, the key scales and
-// the digit weights (vsc), G_t and G_m/G_t. Returns beta_t and the value scale of token t = lane.
+// The new token of the step as loaded (lane l holds elements CPL*l .. CPL*l + CPL-1), with a_t and beta_t.
+template <int CPL>
+struct TokenIn {
+  float kx[CPL], vx[CPL], qx[CPL], an, bn;
+};
+
+// Loads of a unit that do not depend on its buffer count: the scales and zero points (asynchronous copies
+// into shared memory) and the new token (registers).
 template <int D, int G>
-__device__ void dm_stage(const PaceDev &st, const PaceIO &io, int unit, int m0, int has_token, const MmaShared &sh,
-                         float &bt, float &sv_out) {
+__device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, int unit, int has_token,
+                                         const MmaShared &sh, TokenIn<D / 32> &tin) {
   constexpr int CPL = D / 32, NG = D / G;
+  const int lane = threadIdx.x & 31;
+  const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
+  for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(sh.ssc) + 16 * c, gs + 16 * c);
+  if (st.zero_point) {
+    const char *gz = reinterpret_cast<const char *>(st.zp + (size_t)unit * NG * D);
+    for (int c = lane; c < NG * D / 16; c += 32) cp_async16(sh.szp + 16 * c, gz + 16 * c);
+  }
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) tin.kx[c] = tin.vx[c] = tin.qx[c] = 0.0f;
+  tin.an = tin.bn = 0.0f;
+  if (has_token) {
+    const size_t e0 = (size_t)unit * D + CPL * lane;
+    dm_load_io<CPL>(io.k, e0, st.io, tin.kx);
+    dm_load_io<CPL>(io.v, e0, st.io, tin.vx);
+    dm_load_io<CPL>(io.q, e0, st.io, tin.qx);
+    tin.an = io.a[unit];
+    tin.bn = io.beta[unit];
+  }
+}
+
+// Stage the unit: the buffered tokens (asynchronous copies, all in flight at once: int8 keys straight into
+// their rows, packed int4 keys of the mixed buffer into a scratch area first) and the new one (written into
+// buffer slot m0). Leaves in shared memory the key rows (then the q digits), the values, a_t, the key
+// scales and the digit weights (vsc), G_t and G_m/G_t. Returns beta_t and the value scale of token t = lane.
+template <int D, int G>
+__device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, const TokenIn<D / 32> &tin,
+                         const MmaShared &sh, float &bt, float &sv_out) {
+  constexpr int CPL = D / 32;
   const int lane = threadIdx.x & 31;
   const int col0 = CPL * lane;
   const int dP = st.dP;
   const int mt = m0 + has_token;
   const int mixed = st.buf_mode == PACE_BUF_MIXED;
-  // asynchronous 16-byte copies, all in flight at once: scales, zero points, buffered rows (int8 keys
-  // straight into their rows, packed int4 keys of the mixed buffer into a scratch area first)
-  {
-    const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
-    for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(sh.ssc) + 16 * c, gs + 16 * c);
-    if (st.zero_point) {
-      const char *gz = reinterpret_cast<const char *>(st.zp + (size_t)unit * NG * D);
-      for (int c = lane; c < NG * D / 16; c += 32) cp_async16(sh.szp + 16 * c, gz + 16 * c);
-    }
-  }
   const int rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
   unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
   if (m0 > 0) {
@@ -301,16 +324,8 @@ __device__ void dm_stage(const PaceDev &st, const PaceIO &io, int unit, int m0, 
     const float4 r = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
     sa = r.x; sb = r.y; ssk = r.z; ssv = r.w;
   }
-  float kx[CPL], vx[CPL], qx[CPL], an = 0.0f, bn = 0.0f;
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) kx[c] = vx[c] = qx[c] = 0.0f;
-  if (has_token) {
-    dm_load_io<CPL>(io.k, (size_t)unit * D + col0, st.io, kx);
-    dm_load_io<CPL>(io.v, (size_t)unit * D + col0, st.io, vx);
-    dm_load_io<CPL>(io.q, (size_t)unit * D + col0, st.io, qx);
-    an = io.a[unit];
-    bn = io.beta[unit];
-  }
+  const float *kx = tin.kx, *vx = tin.vx, *qx = tin.qx;
+  const float an = tin.an, bn = tin.bn;
   cp_async_wait_all();
   __syncwarp();
   if (mixed) {
@@ -504,7 +519,7 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, 
 }
 
 template <int D, int G, int BITS>
-__device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int m0, int has_token,
+__device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
                         const MmaShared &sh) {
   constexpr int NG = D / G, NPP = D / 64, KSG = G / 16, PL = BITS / 4;
   constexpr int NKG = G / 8;            // key n-tiles (8 keys) per group
@@ -513,24 +528,34 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   constexpr int OFF = 1 << (BITS - 1);  // symmetric code offset
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int dP = st.dP;
-  const int mt = m0 + has_token;
-  const int do_flush = !has_token || mt == dP;
-  const int nv = mt + (has_token ? 3 : 0);
-  const int nvt = (nv + 15) >> 4;
-  const int dpp = dm_dpp(dP);
-  const int mixed = st.buf_mode == PACE_BUF_MIXED;
   const int zpm = st.zero_point;
   uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
                               : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
   __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
   uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
 
-  if (lane == 0) prefetch_l2(codes, PL * PLANE * 4);   // the unit's code words start moving right away
-  // the lane's packed words of the first column block load while the buffer is staged
+  // everything that does not depend on the buffer count is in flight before the count is read: the unit's
+  // code words (into L2, and the first column block into registers), scales, zero points, the new token
+  if (lane == 0) prefetch_l2(codes, PL * PLANE * 4);
   uint32_t cw[PL][2][NPP][4];
   dm_load_block<D, PL>(codes, 0, lane, cw);
+  TokenIn<D / 32> tin;
+  dm_issue<D, G>(st, io, unit, has_token, sh, tin);
+  const int m0 = st.m[unit];
+  if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
+    cp_async_wait_all();                         // nothing may land in shared memory after the warp leaves
+    if (has_token && m0 != 0)                    // corrupted counter: leave the unit, emit zeros
+      for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
+    return;                                      // (or a flush with nothing pending)
+  }
+  const int mt = m0 + has_token;
+  const int do_flush = !has_token || mt == dP;
+  const int nv = mt + (has_token ? 3 : 0);
+  const int nvt = (nv + 15) >> 4;
+  const int dpp = dm_dpp(dP);
+  const int mixed = st.buf_mode == PACE_BUF_MIXED;
   float bt, sv;
-  dm_stage<D, G>(st, io, unit, m0, has_token, sh, bt, sv);
+  dm_stage<D, G>(st, unit, m0, has_token, tin, sh, bt, sv);
   dm_tables<D, G>(sh, nv, mt, dP, dpp, has_token, do_flush, bt, sv);
   const float gm = sh.gam[mt - 1];
   const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;
@@ -654,6 +679,23 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const int jl = 16 * m + g8;              // local columns jl (hi = 0) and jl + 8 (hi = 1)
+      // A: the three bf16 parts of rho_s u_s,j for tokens s = 8sb + 2tq, +1 and columns jl, jl + 8
+      auto parts = [&](int sb, uint32_t (&ap)[3][2]) {
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int s0 = 8 * sb + 2 * tq;
+          const float x0 = s0 < mt ? sh.ck[s0] * sh.ub[s0 * UB_STRIDE + jl + 8 * hi] : 0.0f;
+          const float x1 = s0 + 1 < mt ? sh.ck[s0 + 1] * sh.ub[(s0 + 1) * UB_STRIDE + jl + 8 * hi] : 0.0f;
+          const uint32_t p0 = bf16x2_bits(x0, x1);
+          const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
+          const uint32_t p1 = bf16x2_bits(r0, r1);
+          ap[0][hi] = p0;
+          ap[1][hi] = p1;
+          ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
+        }
+      };
+      uint32_t ap0[3][2];                      // tokens 0..7: shared by the groups of the M-tile
+      parts(0, ap0);
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
         float fs[2], fz[2];
@@ -664,24 +706,8 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
           fz[hi] = -(8388608.0f + (float)(zpm ? (int)sh.szp[gi * D + j] : OFF));
         }
         float c[NKG][4];
-        // A: the three bf16 parts of rho_s u_s,j for tokens s = 8sb + 2tq, +1 and columns jl, jl + 8
-        auto parts = [&](int sb, uint32_t (&ap)[3][2]) {
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int s0 = 8 * sb + 2 * tq;
-            const float x0 = s0 < mt ? sh.ck[s0] * sh.ub[s0 * UB_STRIDE + jl + 8 * hi] : 0.0f;
-            const float x1 = s0 + 1 < mt ? sh.ck[s0 + 1] * sh.ub[(s0 + 1) * UB_STRIDE + jl + 8 * hi] : 0.0f;
-            const uint32_t p0 = bf16x2_bits(x0, x1);
-            const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
-            const uint32_t p1 = bf16x2_bits(r0, r1);
-            ap[0][hi] = p0;
-            ap[1][hi] = p1;
-            ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
-          }
-        };
         {
-          uint32_t ap[3][2];
-          parts(0, ap);
+          const uint32_t(&ap)[3][2] = ap0;
           const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
 #pragma unroll
           for (int nn = 0; nn < NKG; ++nn) {
@@ -766,7 +792,7 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
               const float2 y = __fadd2_rn(__fmul2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2), mg2);
               uint32_t pair;
               if (!zpm) {
-                pair = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410) & 0x00FF00FFu;
+                pair = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410);   // bytes 1, 3 are 0
               } else {
                 const int c0 = min(max((int)(__float_as_uint(y.x) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
                 const int c1 = min(max((int)(__float_as_uint(y.y) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
@@ -795,6 +821,8 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
           *reinterpret_cast<uint4 *>(codes + pl * PLANE + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4) =
               make_uint4(cw[pl][m][pp][0], cw[pl][m][pp][1], cw[pl][m][pp][2], cw[pl][m][pp][3]);
   }
+  __syncwarp();
+  if (lane == 0) st.m[unit] = do_flush ? 0 : mt;
 }
 
 // One launch per code pool (int4 heads, int8 heads), so that each path gets its own register allocation
@@ -803,25 +831,15 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 template <int D, int G, int BITS>
 __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int HP = BITS == 4 ? st.H4 : st.H8;
   const int w = blockIdx.x * DM_WARPS + warp;
   if (w >= st.B * HP) return;
   const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
-  const int u = b * st.H + h;
-  const int m0 = st.m[u];
-  if (m0 < 0 || m0 >= st.dP) {                  // corrupted counter: leave the unit, emit zeros
-    if (has_token)
-      for (int c = lane; c < D; c += 32) store_io(io.o, (long)u * D + c, 0.0f, st.io);
-    return;
-  }
-  if (!has_token && m0 == 0) return;            // flush with nothing pending
   const MmaSmem L = mma_smem(D, G, st.dP, st.buf_mode == PACE_BUF_MIXED, st.zero_point);
   const MmaShared sh = mma_shared(smem + (size_t)warp * L.total, L, st.dP);
-  dm_unit<D, G, BITS>(st, io, b, h, u, m0, has_token, sh);
-  __syncwarp();
-  if (lane == 0) st.m[u] = (!has_token || m0 + 1 == st.dP) ? 0 : m0 + 1;
+  dm_unit<D, G, BITS>(st, io, b, h, b * st.H + h, has_token, sh);
 }
 
 template <int D, int G, int BITS>
