@@ -395,10 +395,8 @@ def main():
     if dist:
         dist.barrier()
     setup, ms, R = measure(P, torch, wl, P.PACE_STATE_QUANT, K, W, sampler)
-    ms_t = torch.tensor([ms], device="cuda")
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    from bit_gated_delta_gb300 import shard
+    ms_max = shard.max_over_ranks(ms, dist)      # weak scaling: each rank owns its B sequences
     value = world * wl.B / (ms_max * 1e-3)
     units = wl.B * wl.H
     alg = units * decode_bytes_period_avg(wl.d_k, wl.g, wl.dP)
