@@ -357,13 +357,42 @@ def rotation_count(nbytes: int, dP: int, align_dp: bool) -> int:
     return int(R)
 
 
-def measure(P, torch, wl, state_mode, K, W, sampler=None):
+def measure(P, torch, wl, state_mode, K, W, sampler=None, min_sets=2):
     bytes1 = P.pace_state_bytes(P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, state_mode=state_mode,
                                               buf_mode=P.PACE_BUF_INT8))
-    R = rotation_count(bytes1, wl.dP, state_mode == P.PACE_STATE_QUANT)
+    R = max(rotation_count(bytes1, wl.dP, state_mode == P.PACE_STATE_QUANT), min_sets)
+    if state_mode == P.PACE_STATE_QUANT:
+        R = -(-R // wl.dP) * wl.dP
     setup = DecodeSetup(P, torch, wl, state_mode, R)
     ms = time_steps(torch, setup, K, W, sampler)
     return setup, ms, R
+
+
+def batch_sweep(P, torch, token_steps=100):
+    """The pages' throughput study shape: 24 gated-delta layers x 16 heads, one token step = 24 sequential layer
+    launches (each layer its own state set, in one CUDA graph); PACE-4 dP=8 against the per-token bf16 kernel at
+    every batch size. Returns per-batch tokens/s of both and the smallest batch from which PACE-4 stays faster."""
+    import synth
+    out, L = {}, 24
+    for b in (1, 2, 4, 8, 16, 32, 64, 128):
+        wl = synth.workload("sweep", B=b)
+        row = {}
+        for name, mode in (("pace4", P.PACE_STATE_QUANT), ("bf16", P.PACE_STATE_BF16)):
+            s, ms, R = measure(P, torch, wl, mode, token_steps * L, 3 * L, min_sets=L)
+            row[f"{name}_tokens_per_s"] = b / (ms * L * 1e-3)
+            row[f"{name}_ms_per_token_step"] = ms * L
+            s.close()
+            torch.cuda.empty_cache()
+        row["speedup"] = row["pace4_tokens_per_s"] / row["bf16_tokens_per_s"]
+        out[str(b)] = row
+    faster = [int(b) for b, r in out.items() if r["speedup"] > 1.0]
+    cross = None
+    for b in sorted(int(x) for x in out):
+        if all(out[str(c)]["speedup"] > 1.0 for c in out if int(c) >= b):
+            cross = b
+            break
+    return {"layers": L, "heads": 16, "d": 128, "per_batch": out, "pace4_faster_from_batch": cross,
+            "note": "one token step = 24 layer launches on distinct state sets; >= 24 sets rotate"}
 
 
 def main():
@@ -431,6 +460,7 @@ def main():
                                        "frac": alg3 / (ms3 * 1e-3) / 1e9 / peak}
                 s3.close()
             torch.cuda.empty_cache()
+        extra["sweep_24x16"] = batch_sweep(P, torch)
 
     cb = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:

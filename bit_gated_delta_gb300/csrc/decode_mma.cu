@@ -270,13 +270,28 @@ __device__ __forceinline__ void dm_load_block(const uint32_t *codes, int cb, int
 template <int CPL>
 struct TokenIn {
   float kx[CPL], vx[CPL], qx[CPL], an, bn;
+  float4 bs;   // buffered token `lane`: a, beta, key scale, value scale (when prefetched)
+  int pre;     // buffered rows already in flight (0: the staging issues the count's rows itself)
 };
+
+// Asynchronous copies of buffered rows 0 .. n-1 of a unit into shared memory: int8 keys straight into their
+// rows, packed int4 keys of the mixed buffer into a scratch area (the fp16 row area, built later).
+template <int D>
+__device__ __forceinline__ void dm_issue_rows(const PaceDev &st, int unit, int n, const MmaShared &sh) {
+  const int lane = threadIdx.x & 31, dP = st.dP, mixed = st.buf_mode == PACE_BUF_MIXED;
+  const int rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
+  unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
+  const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
+  const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
+  for (int c = lane; c < n * rk / 16; c += 32) cp_async16(kdst + 16 * c, gk + 16 * c);
+  for (int c = lane; c < n * rv / 16; c += 32) cp_async16(sh.vrow + 16 * c, gv + 16 * c);
+}
 
 // Loads of a unit that do not depend on its buffer count: the scales and zero points (asynchronous copies
 // into shared memory) and the new token (registers).
 template <int D, int G>
 __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, int unit, int has_token,
-                                         const MmaShared &sh, TokenIn<D / 32> &tin) {
+                                         const MmaShared &sh, TokenIn<D / 32> &tin, int pre = 0) {
   constexpr int CPL = D / 32, NG = D / G;
   const int lane = threadIdx.x & 31;
   const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
@@ -296,6 +311,12 @@ __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, in
     tin.an = io.a[unit];
     tin.bn = io.beta[unit];
   }
+  tin.pre = pre;
+  tin.bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (pre > 0) {                                 // small batches: every buffered row, before the count is known
+    dm_issue_rows<D>(st, unit, pre, sh);
+    if (lane < pre) tin.bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * st.dP + lane) * 4);
+  }
 }
 
 // Stage the unit: the buffered tokens (asynchronous copies, all in flight at once: int8 keys straight into
@@ -311,17 +332,11 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
   const int dP = st.dP;
   const int mt = m0 + has_token;
   const int mixed = st.buf_mode == PACE_BUF_MIXED;
-  const int rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
   unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
-  if (m0 > 0) {
-    const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
-    const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
-    for (int c = lane; c < m0 * rk / 16; c += 32) cp_async16(kdst + 16 * c, gk + 16 * c);
-    for (int c = lane; c < m0 * rv / 16; c += 32) cp_async16(sh.vrow + 16 * c, gv + 16 * c);
-  }
+  if (tin.pre == 0 && m0 > 0) dm_issue_rows<D>(st, unit, m0, sh);
   float sa = 0.0f, sb = 0.0f, ssk = 0.0f, ssv = 0.0f;
   if (lane < m0) {
-    const float4 r = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
+    const float4 r = tin.pre ? tin.bs : *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
     sa = r.x; sb = r.y; ssk = r.z; ssv = r.w;
   }
   const float *kx = tin.kx, *vx = tin.vx, *qx = tin.qx;
@@ -518,15 +533,295 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, 
   __syncwarp();
 }
 
+// One 32-column block cb of a unit: the dots, the replay and readout of its columns and, at a rounding step,
+// their requantization. sh holds the unit's tables; its pb and ub are the calling warp's own. With next_block
+// set, the words of block cb + 1 are loaded into cw as soon as this block's dots are done with them (steps
+// without rounding).
 template <int D, int G, int BITS>
-__device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
-                        const MmaShared &sh) {
+__device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, int unit, int cb, int m0, int has_token,
+                                         uint32_t *codes, __nv_bfloat16 *scale, uint8_t *zpt, const MmaShared &sh,
+                                         uint32_t (&cw)[BITS / 4][2][D / 64][4], bool next_block) {
   constexpr int NG = D / G, NPP = D / 64, KSG = G / 16, PL = BITS / 4;
   constexpr int NKG = G / 8;            // key n-tiles (8 keys) per group
   constexpr int NH = BITS == 8 ? 2 : 1, NPN = 4 / NH;   // dot passes, column n-tiles per pass
   constexpr uint32_t PLANE = D * D / 8; // words per nibble plane
   constexpr int OFF = 1 << (BITS - 1);  // symmetric code offset
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
+  const int dP = st.dP;
+  const int zpm = st.zero_point;
+  const int mt = m0 + has_token;
+  const int do_flush = !has_token || mt == dP;
+  const int nv = mt + (has_token ? 3 : 0);
+  const int nvt = (nv + 15) >> 4;
+  const int dpp = dm_dpp(dP);
+  const int mixed = st.buf_mode == PACE_BUF_MIXED;
+  const float gm = sh.gam[mt - 1];
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;
+
+  // ---- dots: P[v][j] for the 32 columns of the block; n-tile n = columns cb*32 + 8n .. +7
+#pragma unroll 1
+  for (int vt = 0; vt < nvt; ++vt) {
+    const int v0 = 16 * vt + g8;
+    const int ar = 16 * vt + arow;
+    float pacc[4][4];
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh)          // int8 heads: two passes of two n-tiles (register budget)
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        uint32_t sc[NPN], zz[NPN];
+#pragma unroll
+        for (int q = 0; q < NPN; ++q) {
+          const int j = cb * 32 + 8 * (nh * NPN + q) + 2 * tq;
+          sc[q] = *reinterpret_cast<const uint32_t *>(sh.ssc + gi * D + j);
+          zz[q] = zpm ? (uint32_t)*reinterpret_cast<const uint16_t *>(sh.szp + gi * D + j) : 0u;
+        }
+        float dacc[PL][NPN][4];
+#pragma unroll
+        for (int kk = 0; kk < KSG; ++kk) {
+          const int ks = gi * KSG + kk;
+          uint32_t a[4];
+          ldsm_x4(a, sh.ah + ah_off<D>(ar, 2 * ks + acol));
+#pragma unroll
+          for (int q = 0; q < NPN; ++q)
+#pragma unroll
+            for (int pl = 0; pl < PL; ++pl) {
+              const int n = nh * NPN + q;
+              uint32_t w = cw[pl][n >> 1][ks >> 2][(n & 1) * 2 + ((ks >> 1) & 1)];
+              if (ks & 1) w >>= 8;
+              const uint32_t b0 = (w & 0x000F000Fu) | 0x64006400u, b1 = (w & 0x00F000F0u) | 0x64006400u;
+              if (kk == 0) mma_f16_z(dacc[pl][q], a, b0, b1); else mma_f16(dacc[pl][q], a, b0, b1);
+            }
+        }
+        // fold the group: P += s_gj (D - T1 - z_gj T2)
+        const float2 c0 = sh.cf[v0 * 4 + gi], c1 = sh.cf[(v0 + 8) * 4 + gi];
+        const float k0 = fmaf((float)OFF, c0.y, c0.x), k1 = fmaf((float)OFF, c1.y, c1.x);
+#pragma unroll
+        for (int q = 0; q < NPN; ++q) {
+          const int n = nh * NPN + q;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float s = (e & 1) ? bf16_hi(sc[q]) : bf16_lo(sc[q]);
+            const float2 c = (e >> 1) ? c1 : c0;
+            float tot;
+            if (BITS == 4) {
+              if (!zpm)
+                tot = dacc[0][q][e] - ((e >> 1) ? k1 : k0);
+              else
+                tot = dacc[0][q][e] - fmaf((float)((zz[q] >> (8 * (e & 1))) & 0xFFu), c.y, c.x);
+            } else {
+              const int zj = zpm ? (int)((zz[q] >> (8 * (e & 1))) & 0xFFu) : OFF;
+              tot = (float)(__float2int_rn(dacc[0][q][e]) + 16 * __float2int_rn(dacc[PL - 1][q][e]) -
+                            17 * __float2int_rn(c.x) - zj * __float2int_rn(c.y));
+            }
+            pacc[n][e] = gi == 0 ? s * tot : fmaf(s, tot, pacc[n][e]);
+          }
+        }
+      }
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      if (v0 < nv) *reinterpret_cast<float2 *>(sh.pb + v0 * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][0], pacc[n][1]);
+      if (v0 + 8 < nv)
+        *reinterpret_cast<float2 *>(sh.pb + (v0 + 8) * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][2], pacc[n][3]);
+    }
+  }
+  // without a flush the block's words are done with: the next block's load overlaps the replay
+  if (next_block && !do_flush && cb + 1 < D / 32) dm_load_block<D, PL>(codes, cb + 1, lane, cw);
+  __syncwarp();
+
+  // ---- replay and readout: lane = column cb*32 + lane
+  {
+    const int j = cb * 32 + lane;
+    auto value = [&](int t, float svt) -> float {
+      if (mixed) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(sh.vrow)[t * D + j]);
+      return svt * (float)reinterpret_cast<const int8_t *>(sh.vrow)[t * D + j];
+    };
+    float o = 0.0f;
+    if (has_token)
+      o = gm * (sh.vsc[mt] * sh.pb[mt * PB_STRIDE + lane] +
+                (sh.vsc[mt + 1] * sh.pb[(mt + 1) * PB_STRIDE + lane] + sh.vsc[mt + 2] * sh.pb[(mt + 2) * PB_STRIDE + lane]));
+    if (dP <= 8) {                           // u in registers
+      float u[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        u[t] = 0.0f;
+        if (t < mt) {
+          const float4 tk = sh.tk[t];          // G_t s_kt, beta_t, s_vt, readout coefficient
+          float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
+#pragma unroll
+          for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * 8 + s2], u[s2], acc);
+          u[t] = tk.y * acc;
+          o = fmaf(tk.w, u[t], o);
+          if (do_flush) sh.ub[t * UB_STRIDE + lane] = u[t];
+        }
+      }
+    } else {
+      for (int t = 0; t < mt; ++t) {
+        const float4 tk = sh.tk[t];
+        float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
+        for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * dP + s2], sh.ub[s2 * UB_STRIDE + lane], acc);
+        const float ut = tk.y * acc;
+        sh.ub[t * UB_STRIDE + lane] = ut;
+        o = fmaf(tk.w, ut, o);
+      }
+    }
+    if (has_token) store_io(io.o, (long)unit * D + j, o, st.io);
+  }
+  __syncwarp();
+  if (!do_flush) return;
+
+  // ---- flush: rebuild and requantize the block's columns, M-tile by M-tile, group by group
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int jl = 16 * m + g8;              // local columns jl (hi = 0) and jl + 8 (hi = 1)
+    // A: the three bf16 parts of rho_s u_s,j for tokens s = 8sb + 2tq, +1 and columns jl, jl + 8
+    auto parts = [&](int sb, uint32_t (&ap)[3][2]) {
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int s0 = 8 * sb + 2 * tq;
+        const float x0 = s0 < mt ? sh.ck[s0] * sh.ub[s0 * UB_STRIDE + jl + 8 * hi] : 0.0f;
+        const float x1 = s0 + 1 < mt ? sh.ck[s0 + 1] * sh.ub[(s0 + 1) * UB_STRIDE + jl + 8 * hi] : 0.0f;
+        const uint32_t p0 = bf16x2_bits(x0, x1);
+        const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
+        const uint32_t p1 = bf16x2_bits(r0, r1);
+        ap[0][hi] = p0;
+        ap[1][hi] = p1;
+        ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
+      }
+    };
+    uint32_t ap0[3][2];                      // tokens 0..7: shared by the groups of the M-tile
+    parts(0, ap0);
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      float fs[2], fz[2];
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int j = cb * 32 + jl + 8 * hi;
+        fs[hi] = gm * __bfloat162float(sh.ssc[gi * D + j]);
+        fz[hi] = -(8388608.0f + (float)(zpm ? (int)sh.szp[gi * D + j] : OFF));
+      }
+      float c[NKG][4];
+      {
+        const uint32_t(&ap)[3][2] = ap0;
+        const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
+#pragma unroll
+        for (int nn = 0; nn < NKG; ++nn) {
+          const uint32_t bk = sh.kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + tq];
+          mma_bf16_z(c[nn], a16, bk, bk);
+          mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
+        }
+      }
+#pragma unroll 1
+      for (int sb = 1; sb < (dpp >> 3); ++sb) {
+        uint32_t ap[3][2];
+        parts(sb, ap);
+        const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
+#pragma unroll
+        for (int nn = 0; nn < NKG; ++nn) {
+          const uint32_t bk = sh.kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + 4 * sb + tq];
+          mma_bf16(c[nn], a16, bk, bk);
+          mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
+        }
+      }
+      // the old state: x = G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
+#pragma unroll
+      for (int nn = 0; nn < NKG; ++nn) {
+        const int nk = gi * NKG + nn, r = nk & 3;
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int wi = hi * 2 + ((nk >> 2) & 1);
+          uint32_t m16 = (cw[0][m][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu;
+          if (BITS == 8) m16 |= ((cw[PL - 1][m][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu) << 4;
+          const float2 f = make_float2(__uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7610)),
+                                       __uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7632)));
+          const float2 d = __fadd2_rn(f, make_float2(fz[hi], fz[hi]));
+          const float2 x = __ffma2_rn(make_float2(fs[hi], fs[hi]), d, make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]));
+          c[nn][2 * hi] = x.x;
+          c[nn][2 * hi + 1] = x.y;
+        }
+      }
+      // requantize the group for both columns; the lane's keys fill its own words
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        float s;
+        int z;
+        if (!zpm) {
+          float A = 0.0f;
+#pragma unroll
+          for (int nn = 0; nn < NKG; ++nn) A = fmax3(A, fabsf(c[nn][2 * hi]), fabsf(c[nn][2 * hi + 1]));
+          A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 1));
+          A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 2));
+          constexpr float QMAX = (float)(OFF - 1);
+          s = bf16_quot(A, QMAX, 1.0f / QMAX);
+          z = OFF;
+        } else {
+          float lo = 0.0f, hi_ = 0.0f;
+#pragma unroll
+          for (int nn = 0; nn < NKG; ++nn) {
+            lo = fmin3(lo, c[nn][2 * hi], c[nn][2 * hi + 1]);
+            hi_ = fmax3(hi_, c[nn][2 * hi], c[nn][2 * hi + 1]);
+          }
+          lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+          hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 1));
+          lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
+          hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 2));
+          constexpr float QM = (float)((1 << BITS) - 1);
+          s = bf16_quot(__fsub_rn(hi_, lo), QM, 1.0f / QM);
+          z = 0;
+          if (s >= FLT_MIN) z = min(max(__float2int_rn(__fmul_rn(-lo, rcp_bf16(s))), 0), (1 << BITS) - 1);
+        }
+        if (!(s >= FLT_MIN)) s = 0.0f;
+        const float r = s > 0.0f ? rcp_bf16(s) : 0.0f;
+        // codes: rint(x r) by the 1.5 * 2^23 rounding constant (symmetric: the clamp to +-qmax never binds,
+        // since s = bf16(A / qmax) puts |x r| below qmax + 1/2); zero point: + z, clamp to [0, 2^b - 1]
+        const float2 r2 = make_float2(r, r);
+        const float mg = zpm ? 12582912.0f : 12582912.0f + (float)OFF;
+        const float2 mg2 = make_float2(mg, mg);
+#pragma unroll
+        for (int pw = 0; pw < G / 32; ++pw) {
+          const int p = gi * (G / 32) + pw;  // 32-key span
+          uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int nn = 4 * pw + rr;
+            const float2 y = __fadd2_rn(__fmul2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2), mg2);
+            uint32_t pair;
+            if (!zpm) {
+              pair = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410);   // bytes 1, 3 are 0
+            } else {
+              const int c0 = min(max((int)(__float_as_uint(y.x) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
+              const int c1 = min(max((int)(__float_as_uint(y.y) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
+              pair = __byte_perm((uint32_t)c0, (uint32_t)c1, 0x5410);
+            }
+            w0 += (pair & 0x000F000Fu) << (4 * rr);
+            if (BITS == 8) w1 += ((pair >> 4) & 0x000F000Fu) << (4 * rr);
+          }
+          cw[0][m][p >> 1][hi * 2 + (p & 1)] = w0;
+          if (BITS == 8) cw[PL - 1][m][p >> 1][hi * 2 + (p & 1)] = w1;
+        }
+        if (tq == 0) {
+          const int j = cb * 32 + jl + 8 * hi;
+          scale[gi * D + j] = __float2bfloat16_rn(s);
+          if (zpm) zpt[gi * D + j] = (uint8_t)z;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int pl = 0; pl < PL; ++pl)
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int pp = 0; pp < NPP; ++pp)
+        *reinterpret_cast<uint4 *>(codes + pl * PLANE + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4) =
+            make_uint4(cw[pl][m][pp][0], cw[pl][m][pp][1], cw[pl][m][pp][2], cw[pl][m][pp][3]);
+}
+
+template <int D, int G, int BITS>
+__device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
+                        const MmaShared &sh) {
+  constexpr int NG = D / G, NPP = D / 64, PL = BITS / 4;
+  constexpr uint32_t PLANE = D * D / 8; // words per nibble plane
+  const int lane = threadIdx.x & 31;
   const int dP = st.dP;
   const int zpm = st.zero_point;
   uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
@@ -551,275 +846,15 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
   const int nv = mt + (has_token ? 3 : 0);
-  const int nvt = (nv + 15) >> 4;
   const int dpp = dm_dpp(dP);
-  const int mixed = st.buf_mode == PACE_BUF_MIXED;
   float bt, sv;
   dm_stage<D, G>(st, unit, m0, has_token, tin, sh, bt, sv);
   dm_tables<D, G>(sh, nv, mt, dP, dpp, has_token, do_flush, bt, sv);
-  const float gm = sh.gam[mt - 1];
-  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;
 
 #pragma unroll 1
   for (int cb = 0; cb < D / 32; ++cb) {
     if (cb > 0 && do_flush) dm_load_block<D, PL>(codes, cb, lane, cw);
-
-    // ---- dots: P[v][j] for the 32 columns of the block; n-tile n = columns cb*32 + 8n .. +7
-#pragma unroll 1
-    for (int vt = 0; vt < nvt; ++vt) {
-      const int v0 = 16 * vt + g8;
-      const int ar = 16 * vt + arow;
-      float pacc[4][4];
-#pragma unroll
-      for (int nh = 0; nh < NH; ++nh)          // int8 heads: two passes of two n-tiles (register budget)
-#pragma unroll
-        for (int gi = 0; gi < NG; ++gi) {
-          uint32_t sc[NPN], zz[NPN];
-#pragma unroll
-          for (int q = 0; q < NPN; ++q) {
-            const int j = cb * 32 + 8 * (nh * NPN + q) + 2 * tq;
-            sc[q] = *reinterpret_cast<const uint32_t *>(sh.ssc + gi * D + j);
-            zz[q] = zpm ? (uint32_t)*reinterpret_cast<const uint16_t *>(sh.szp + gi * D + j) : 0u;
-          }
-          float dacc[PL][NPN][4];
-#pragma unroll
-          for (int kk = 0; kk < KSG; ++kk) {
-            const int ks = gi * KSG + kk;
-            uint32_t a[4];
-            ldsm_x4(a, sh.ah + ah_off<D>(ar, 2 * ks + acol));
-#pragma unroll
-            for (int q = 0; q < NPN; ++q)
-#pragma unroll
-              for (int pl = 0; pl < PL; ++pl) {
-                const int n = nh * NPN + q;
-                uint32_t w = cw[pl][n >> 1][ks >> 2][(n & 1) * 2 + ((ks >> 1) & 1)];
-                if (ks & 1) w >>= 8;
-                const uint32_t b0 = (w & 0x000F000Fu) | 0x64006400u, b1 = (w & 0x00F000F0u) | 0x64006400u;
-                if (kk == 0) mma_f16_z(dacc[pl][q], a, b0, b1); else mma_f16(dacc[pl][q], a, b0, b1);
-              }
-          }
-          // fold the group: P += s_gj (D - T1 - z_gj T2)
-          const float2 c0 = sh.cf[v0 * 4 + gi], c1 = sh.cf[(v0 + 8) * 4 + gi];
-          const float k0 = fmaf((float)OFF, c0.y, c0.x), k1 = fmaf((float)OFF, c1.y, c1.x);
-#pragma unroll
-          for (int q = 0; q < NPN; ++q) {
-            const int n = nh * NPN + q;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float s = (e & 1) ? bf16_hi(sc[q]) : bf16_lo(sc[q]);
-              const float2 c = (e >> 1) ? c1 : c0;
-              float tot;
-              if (BITS == 4) {
-                if (!zpm)
-                  tot = dacc[0][q][e] - ((e >> 1) ? k1 : k0);
-                else
-                  tot = dacc[0][q][e] - fmaf((float)((zz[q] >> (8 * (e & 1))) & 0xFFu), c.y, c.x);
-              } else {
-                const int zj = zpm ? (int)((zz[q] >> (8 * (e & 1))) & 0xFFu) : OFF;
-                tot = (float)(__float2int_rn(dacc[0][q][e]) + 16 * __float2int_rn(dacc[PL - 1][q][e]) -
-                              17 * __float2int_rn(c.x) - zj * __float2int_rn(c.y));
-              }
-              pacc[n][e] = gi == 0 ? s * tot : fmaf(s, tot, pacc[n][e]);
-            }
-          }
-        }
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        if (v0 < nv) *reinterpret_cast<float2 *>(sh.pb + v0 * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][0], pacc[n][1]);
-        if (v0 + 8 < nv)
-          *reinterpret_cast<float2 *>(sh.pb + (v0 + 8) * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][2], pacc[n][3]);
-      }
-    }
-    // without a flush the block's words are done with: the next block's load overlaps the replay
-    if (!do_flush && cb + 1 < D / 32) dm_load_block<D, PL>(codes, cb + 1, lane, cw);
-    __syncwarp();
-
-    // ---- replay and readout: lane = column cb*32 + lane
-    {
-      const int j = cb * 32 + lane;
-      auto value = [&](int t, float svt) -> float {
-        if (mixed) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(sh.vrow)[t * D + j]);
-        return svt * (float)reinterpret_cast<const int8_t *>(sh.vrow)[t * D + j];
-      };
-      float o = 0.0f;
-      if (has_token)
-        o = gm * (sh.vsc[mt] * sh.pb[mt * PB_STRIDE + lane] +
-                  (sh.vsc[mt + 1] * sh.pb[(mt + 1) * PB_STRIDE + lane] + sh.vsc[mt + 2] * sh.pb[(mt + 2) * PB_STRIDE + lane]));
-      if (dP <= 8) {                           // u in registers
-        float u[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          u[t] = 0.0f;
-          if (t < mt) {
-            const float4 tk = sh.tk[t];          // G_t s_kt, beta_t, s_vt, readout coefficient
-            float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
-#pragma unroll
-            for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * 8 + s2], u[s2], acc);
-            u[t] = tk.y * acc;
-            o = fmaf(tk.w, u[t], o);
-            if (do_flush) sh.ub[t * UB_STRIDE + lane] = u[t];
-          }
-        }
-      } else {
-        for (int t = 0; t < mt; ++t) {
-          const float4 tk = sh.tk[t];
-          float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
-          for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * dP + s2], sh.ub[s2 * UB_STRIDE + lane], acc);
-          const float ut = tk.y * acc;
-          sh.ub[t * UB_STRIDE + lane] = ut;
-          o = fmaf(tk.w, ut, o);
-        }
-      }
-      if (has_token) store_io(io.o, (long)unit * D + j, o, st.io);
-    }
-    __syncwarp();
-    if (!do_flush) continue;
-
-    // ---- flush: rebuild and requantize the block's columns, M-tile by M-tile, group by group
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const int jl = 16 * m + g8;              // local columns jl (hi = 0) and jl + 8 (hi = 1)
-      // A: the three bf16 parts of rho_s u_s,j for tokens s = 8sb + 2tq, +1 and columns jl, jl + 8
-      auto parts = [&](int sb, uint32_t (&ap)[3][2]) {
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int s0 = 8 * sb + 2 * tq;
-          const float x0 = s0 < mt ? sh.ck[s0] * sh.ub[s0 * UB_STRIDE + jl + 8 * hi] : 0.0f;
-          const float x1 = s0 + 1 < mt ? sh.ck[s0 + 1] * sh.ub[(s0 + 1) * UB_STRIDE + jl + 8 * hi] : 0.0f;
-          const uint32_t p0 = bf16x2_bits(x0, x1);
-          const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
-          const uint32_t p1 = bf16x2_bits(r0, r1);
-          ap[0][hi] = p0;
-          ap[1][hi] = p1;
-          ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
-        }
-      };
-      uint32_t ap0[3][2];                      // tokens 0..7: shared by the groups of the M-tile
-      parts(0, ap0);
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi) {
-        float fs[2], fz[2];
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int j = cb * 32 + jl + 8 * hi;
-          fs[hi] = gm * __bfloat162float(sh.ssc[gi * D + j]);
-          fz[hi] = -(8388608.0f + (float)(zpm ? (int)sh.szp[gi * D + j] : OFF));
-        }
-        float c[NKG][4];
-        {
-          const uint32_t(&ap)[3][2] = ap0;
-          const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
-#pragma unroll
-          for (int nn = 0; nn < NKG; ++nn) {
-            const uint32_t bk = sh.kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + tq];
-            mma_bf16_z(c[nn], a16, bk, bk);
-            mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
-          }
-        }
-#pragma unroll 1
-        for (int sb = 1; sb < (dpp >> 3); ++sb) {
-          uint32_t ap[3][2];
-          parts(sb, ap);
-          const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
-#pragma unroll
-          for (int nn = 0; nn < NKG; ++nn) {
-            const uint32_t bk = sh.kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + 4 * sb + tq];
-            mma_bf16(c[nn], a16, bk, bk);
-            mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
-          }
-        }
-        // the old state: x = G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
-#pragma unroll
-        for (int nn = 0; nn < NKG; ++nn) {
-          const int nk = gi * NKG + nn, r = nk & 3;
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int wi = hi * 2 + ((nk >> 2) & 1);
-            uint32_t m16 = (cw[0][m][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu;
-            if (BITS == 8) m16 |= ((cw[PL - 1][m][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu) << 4;
-            const float2 f = make_float2(__uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7610)),
-                                         __uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7632)));
-            const float2 d = __fadd2_rn(f, make_float2(fz[hi], fz[hi]));
-            const float2 x = __ffma2_rn(make_float2(fs[hi], fs[hi]), d, make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]));
-            c[nn][2 * hi] = x.x;
-            c[nn][2 * hi + 1] = x.y;
-          }
-        }
-        // requantize the group for both columns; the lane's keys fill its own words
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          float s;
-          int z;
-          if (!zpm) {
-            float A = 0.0f;
-#pragma unroll
-            for (int nn = 0; nn < NKG; ++nn) A = fmax3(A, fabsf(c[nn][2 * hi]), fabsf(c[nn][2 * hi + 1]));
-            A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 1));
-            A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 2));
-            constexpr float QMAX = (float)(OFF - 1);
-            s = bf16_quot(A, QMAX, 1.0f / QMAX);
-            z = OFF;
-          } else {
-            float lo = 0.0f, hi_ = 0.0f;
-#pragma unroll
-            for (int nn = 0; nn < NKG; ++nn) {
-              lo = fmin3(lo, c[nn][2 * hi], c[nn][2 * hi + 1]);
-              hi_ = fmax3(hi_, c[nn][2 * hi], c[nn][2 * hi + 1]);
-            }
-            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
-            hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 1));
-            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
-            hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 2));
-            constexpr float QM = (float)((1 << BITS) - 1);
-            s = bf16_quot(__fsub_rn(hi_, lo), QM, 1.0f / QM);
-            z = 0;
-            if (s >= FLT_MIN) z = min(max(__float2int_rn(__fmul_rn(-lo, rcp_bf16(s))), 0), (1 << BITS) - 1);
-          }
-          if (!(s >= FLT_MIN)) s = 0.0f;
-          const float r = s > 0.0f ? rcp_bf16(s) : 0.0f;
-          // codes: rint(x r) by the 1.5 * 2^23 rounding constant (symmetric: the clamp to +-qmax never binds,
-          // since s = bf16(A / qmax) puts |x r| below qmax + 1/2); zero point: + z, clamp to [0, 2^b - 1]
-          const float2 r2 = make_float2(r, r);
-          const float mg = zpm ? 12582912.0f : 12582912.0f + (float)OFF;
-          const float2 mg2 = make_float2(mg, mg);
-#pragma unroll
-          for (int pw = 0; pw < G / 32; ++pw) {
-            const int p = gi * (G / 32) + pw;  // 32-key span
-            uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-              const int nn = 4 * pw + rr;
-              const float2 y = __fadd2_rn(__fmul2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2), mg2);
-              uint32_t pair;
-              if (!zpm) {
-                pair = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410);   // bytes 1, 3 are 0
-              } else {
-                const int c0 = min(max((int)(__float_as_uint(y.x) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
-                const int c1 = min(max((int)(__float_as_uint(y.y) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
-                pair = __byte_perm((uint32_t)c0, (uint32_t)c1, 0x5410);
-              }
-              w0 += (pair & 0x000F000Fu) << (4 * rr);
-              if (BITS == 8) w1 += ((pair >> 4) & 0x000F000Fu) << (4 * rr);
-            }
-            cw[0][m][p >> 1][hi * 2 + (p & 1)] = w0;
-            if (BITS == 8) cw[PL - 1][m][p >> 1][hi * 2 + (p & 1)] = w1;
-          }
-          if (tq == 0) {
-            const int j = cb * 32 + jl + 8 * hi;
-            scale[gi * D + j] = __float2bfloat16_rn(s);
-            if (zpm) zpt[gi * D + j] = (uint8_t)z;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int pl = 0; pl < PL; ++pl)
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int pp = 0; pp < NPP; ++pp)
-          *reinterpret_cast<uint4 *>(codes + pl * PLANE + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4) =
-              make_uint4(cw[pl][m][pp][0], cw[pl][m][pp][1], cw[pl][m][pp][2], cw[pl][m][pp][3]);
+    dm_block<D, G, BITS>(st, io, unit, cb, m0, has_token, codes, scale, zpt, sh, cw, true);
   }
   __syncwarp();
   if (lane == 0) st.m[unit] = do_flush ? 0 : mt;
@@ -842,19 +877,90 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_mma_k
   dm_unit<D, G, BITS>(st, io, b, h, b * st.H + h, has_token, sh);
 }
 
+// Few units in flight: one CTA per unit. Warp 0 stages the unit and builds its tables in the first work area,
+// then warp w runs column block w with its own dot and replay tables, so a unit's blocks run side by side and
+// the chain of dependent work per unit (the launch time at small batch) is about halved.
+template <int D, int G, int BITS>
+__global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int NG = D / G, NPP = D / 64, PL = BITS / 4, NB = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int HP = BITS == 4 ? st.H4 : st.H8;
+  const int w = blockIdx.x;
+  if (w >= st.B * HP) return;                   // the whole CTA
+  const int b = w / HP, slot = w - b * HP;
+  const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
+  const int unit = b * st.H + h;
+  const int dP = st.dP;
+  const int zpm = st.zero_point;
+  const MmaSmem L = mma_smem(D, G, dP, st.buf_mode == PACE_BUF_MIXED, zpm);
+  const MmaShared sh0 = mma_shared(smem, L, dP);
+  MmaShared shw = sh0;
+  {
+    const MmaShared own = mma_shared(smem + (size_t)warp * L.total, L, dP);
+    shw.pb = own.pb;
+    shw.ub = own.ub;
+  }
+  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
+                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
+  __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
+  uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
+  const bool active = warp < NB;
+  uint32_t cw[PL][2][NPP][4];
+  if (active) dm_load_block<D, PL>(codes, warp, lane, cw);
+  TokenIn<D / 32> tin{};
+  if (warp == 0) dm_issue<D, G>(st, io, unit, has_token, sh0, tin, dP);
+  const int m0 = st.m[unit];
+  if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
+    if (warp == 0) {
+      cp_async_wait_all();                       // nothing may land in shared memory after the CTA leaves
+      if (has_token && m0 != 0)                  // corrupted counter: leave the unit, emit zeros
+        for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
+    }
+    return;
+  }
+  const int mt = m0 + has_token;
+  const int do_flush = !has_token || mt == dP;
+  if (warp == 0) {
+    float bt, sv;
+    dm_stage<D, G>(st, unit, m0, has_token, tin, sh0, bt, sv);
+    dm_tables<D, G>(sh0, mt + (has_token ? 3 : 0), mt, dP, dm_dpp(dP), has_token, do_flush, bt, sv);
+  }
+  __syncthreads();
+  if (active) dm_block<D, G, BITS>(st, io, unit, warp, m0, has_token, codes, scale, zpt, shw, cw, false);
+  __syncthreads();
+  if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
+}
+
+static int dm_sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  return sms;
+}
+
 template <int D, int G, int BITS>
 static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, size_t smem) {
-  auto kern = decode_mma_kernel<D, G, BITS>;
   static size_t opted = 0;
   if (smem > 48 * 1024 && smem > opted) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_split_kernel<D, G, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     opted = 227 * 1024;
   }
   const long units = (long)d.B * (BITS == 4 ? d.H4 : d.H8);
   if (units == 0) return cudaSuccess;
-  const long blocks = (units + DM_WARPS - 1) / DM_WARPS;
-  kern<<<(unsigned)blocks, DM_WARPS * 32, smem, s>>>(d, io, has_token);
+  // one warp per unit while every SM holds 16 units' warps or more; below that, a CTA per unit
+  if (units * DM_WARPS <= (long)dm_sm_count() * 16) {
+    decode_split_kernel<D, G, BITS><<<(unsigned)units, DM_WARPS * 32, smem, s>>>(d, io, has_token);
+  } else {
+    const long blocks = (units + DM_WARPS - 1) / DM_WARPS;
+    decode_mma_kernel<D, G, BITS><<<(unsigned)blocks, DM_WARPS * 32, smem, s>>>(d, io, has_token);
+  }
   return cudaGetLastError();
 }
 
