@@ -24,6 +24,8 @@
 // Between the two, each lane replays one column in reduced form (fp32):
 //   u_t = beta_t (v_t - G_t (S_hat^T k_t) - sum_{s<t} (G_t/G_s)(k_s.k_t) u_s),   G_t = a_1 .. a_t
 //   o   = G_m (S_hat^T q) + sum_s (G_m/G_s)(k_s.q) u_s
+#pragma once
+
 #include <cuda_fp16.h>
 
 #include "pace_common.cuh"
@@ -31,6 +33,9 @@
 namespace pace {
 
 constexpr int DM_WARPS = 4;   // units (warps) per block
+#ifndef PACE_DM_MIN_BLOCKS
+#define PACE_DM_MIN_BLOCKS 4  // resident blocks per SM the int4 kernels are compiled for (register cap)
+#endif
 constexpr int PB_STRIDE = 40; // floats per row of the per-block dot table (conflict-free fragment stores)
 constexpr int UB_STRIDE = 36; // floats per row of the per-block replay table (conflict-free fragment loads)
 
@@ -45,14 +50,14 @@ constexpr RcpTable make_rcp_table() {
   for (int i = 0; i < 128; ++i) t.v[i] = (float)(128.0 / (128 + i));
   return t;
 }
-__device__ const RcpTable g_rcp = make_rcp_table();
+static __device__ const RcpTable g_rcp = make_rcp_table();
 
 __host__ __device__ inline int dm_dpp(int dP) { return 8 * ((dP + 7) / 8); }   // token slots per K part
 __host__ __device__ inline int dm_wstride(int dP) { return dP <= 8 ? 8 : dP; }
 __host__ __device__ inline int dm_nvt(int dP) { return (dP + 3 + 15) / 16; }   // 16-vector tiles
 
 struct MmaSmem {
-  size_t krow, vrow, ah, kbf, pb, ub, W, tk, ck, cf, a, vsc, gam, dmq, ssc, szp, total;
+  size_t krow, vrow, ah, kbf, pb, ub, W, tk, ck, cf, a, vsc, gam, dmq, bet, svt, ssc, szp, total;
 };
 // Per-warp work area.
 __host__ __device__ inline MmaSmem mma_smem(int D, int G, int dP, int mixed, int zp) {
@@ -75,6 +80,8 @@ __host__ __device__ inline MmaSmem mma_smem(int D, int G, int dP, int mixed, int
   L.vsc = carve(off, (size_t)nvmax * 4);
   L.gam = carve(off, (size_t)dP * 4);
   L.dmq = carve(off, (size_t)dP * 4);
+  L.bet = carve(off, (size_t)dP * 4);                     // beta_t and the value scale s_vt (cooperative
+  L.svt = carve(off, (size_t)dP * 4);                     // staging hands them over in shared memory)
   L.ssc = carve(off, (size_t)(D / G) * D * 2);            // the unit's group scales (bf16), as resident
   L.szp = carve(off, zp ? (size_t)(D / G) * D : 0);       // and zero points
   L.total = carve(off, 0, 16);
@@ -90,7 +97,7 @@ struct MmaShared {
   float4 *tk;
   float *ck;
   float2 *cf;
-  float *e3, *a, *vsc, *gam, *dmq;
+  float *e3, *a, *vsc, *gam, *dmq, *bet, *svt;
   __nv_bfloat16 *ssc;
   uint8_t *szp;
 };
@@ -112,6 +119,8 @@ __device__ inline MmaShared mma_shared(unsigned char *base, const MmaSmem &L, in
   s.vsc = reinterpret_cast<float *>(base + L.vsc);
   s.gam = reinterpret_cast<float *>(base + L.gam);
   s.dmq = reinterpret_cast<float *>(base + L.dmq);
+  s.bet = reinterpret_cast<float *>(base + L.bet);
+  s.svt = reinterpret_cast<float *>(base + L.svt);
   s.ssc = reinterpret_cast<__nv_bfloat16 *>(base + L.ssc);
   s.szp = base + L.szp;
   return s;
@@ -122,6 +131,13 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D = A x B + C
+__device__ __forceinline__ void mma_f16_c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
+                                          float c1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%11,%11};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
 // D = A x B (zero accumulator)
 __device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -276,9 +292,10 @@ struct TokenIn {
 
 // Asynchronous copies of buffered rows 0 .. n-1 of a unit into shared memory: int8 keys straight into their
 // rows, packed int4 keys of the mixed buffer into a scratch area (the fp16 row area, built later).
-template <int D>
+template <int D, int MX>
 __device__ __forceinline__ void dm_issue_rows(const PaceDev &st, int unit, int n, const MmaShared &sh) {
-  const int lane = threadIdx.x & 31, dP = st.dP, mixed = st.buf_mode == PACE_BUF_MIXED;
+  constexpr int mixed = MX;
+  const int lane = threadIdx.x & 31, dP = st.dP;
   const int rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
   unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
   const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
@@ -289,14 +306,14 @@ __device__ __forceinline__ void dm_issue_rows(const PaceDev &st, int unit, int n
 
 // Loads of a unit that do not depend on its buffer count: the scales and zero points (asynchronous copies
 // into shared memory) and the new token (registers).
-template <int D, int G>
+template <int D, int G, int ZP, int MX>
 __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, int unit, int has_token,
                                          const MmaShared &sh, TokenIn<D / 32> &tin, int pre = 0) {
   constexpr int CPL = D / 32, NG = D / G;
   const int lane = threadIdx.x & 31;
   const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
   for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(sh.ssc) + 16 * c, gs + 16 * c);
-  if (st.zero_point) {
+  if (ZP) {
     const char *gz = reinterpret_cast<const char *>(st.zp + (size_t)unit * NG * D);
     for (int c = lane; c < NG * D / 16; c += 32) cp_async16(sh.szp + 16 * c, gz + 16 * c);
   }
@@ -314,7 +331,7 @@ __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, in
   tin.pre = pre;
   tin.bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (pre > 0) {                                 // small batches: every buffered row, before the count is known
-    dm_issue_rows<D>(st, unit, pre, sh);
+    dm_issue_rows<D, MX>(st, unit, pre, sh);
     if (lane < pre) tin.bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * st.dP + lane) * 4);
   }
 }
@@ -323,7 +340,7 @@ __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, in
 // their rows, packed int4 keys of the mixed buffer into a scratch area first) and the new one (written into
 // buffer slot m0). Leaves in shared memory the key rows (then the q digits), the values, a_t, the key
 // scales and the digit weights (vsc), G_t and G_m/G_t. Returns beta_t and the value scale of token t = lane.
-template <int D, int G>
+template <int D, int G, int MX>
 __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, const TokenIn<D / 32> &tin,
                          const MmaShared &sh, float &bt, float &sv_out) {
   constexpr int CPL = D / 32;
@@ -331,9 +348,9 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
   const int col0 = CPL * lane;
   const int dP = st.dP;
   const int mt = m0 + has_token;
-  const int mixed = st.buf_mode == PACE_BUF_MIXED;
+  constexpr int mixed = MX;
   unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
-  if (tin.pre == 0 && m0 > 0) dm_issue_rows<D>(st, unit, m0, sh);
+  if (tin.pre == 0 && m0 > 0) dm_issue_rows<D, MX>(st, unit, m0, sh);
   float sa = 0.0f, sb = 0.0f, ssk = 0.0f, ssv = 0.0f;
   if (lane < m0) {
     const float4 r = tin.pre ? tin.bs : *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
@@ -537,7 +554,7 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, 
 // their requantization. sh holds the unit's tables; its pb and ub are the calling warp's own. With next_block
 // set, the words of block cb + 1 are loaded into cw as soon as this block's dots are done with them (steps
 // without rounding).
-template <int D, int G, int BITS>
+template <int D, int G, int BITS, int ZP, int MX>
 __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, int unit, int cb, int m0, int has_token,
                                          uint32_t *codes, __nv_bfloat16 *scale, uint8_t *zpt, const MmaShared &sh,
                                          uint32_t (&cw)[BITS / 4][2][D / 64][4], bool next_block) {
@@ -548,13 +565,13 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
   constexpr int OFF = 1 << (BITS - 1);  // symmetric code offset
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int dP = st.dP;
-  const int zpm = st.zero_point;
+  constexpr int zpm = ZP;
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
   const int nv = mt + (has_token ? 3 : 0);
   const int nvt = (nv + 15) >> 4;
   const int dpp = dm_dpp(dP);
-  const int mixed = st.buf_mode == PACE_BUF_MIXED;
+  constexpr int mixed = MX;
   const float gm = sh.gam[mt - 1];
   const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;
 
@@ -563,6 +580,57 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
   for (int vt = 0; vt < nvt; ++vt) {
     const int v0 = 16 * vt + g8;
     const int ar = 16 * vt + arow;
+    if constexpr (BITS == 4) {
+      // int4: each group's accumulator starts at -(T1 + z T2) (symmetric: z = 8 for every column, so the whole
+      // offset goes in; zero point: -T1, and -z_gj T2 per column after the MMAs). All partial sums are exact
+      // integers below 2^24, so the fold is one rounding per group: P += s_gj * (D_g - T1 - z_gj T2).
+      float2 pacc2[4][2];
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        const float2 c0 = sh.cf[v0 * 4 + gi], c1 = sh.cf[(v0 + 8) * 4 + gi];
+        const float i0 = ZP ? -c0.x : -fmaf((float)OFF, c0.y, c0.x);
+        const float i1 = ZP ? -c1.x : -fmaf((float)OFF, c1.y, c1.x);
+        float dacc[4][4];
+#pragma unroll
+        for (int kk = 0; kk < KSG; ++kk) {
+          const int ks = gi * KSG + kk;
+          uint32_t a[4];
+          ldsm_x4(a, sh.ah + ah_off<D>(ar, 2 * ks + acol));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w = cw[0][q >> 1][ks >> 2][(q & 1) * 2 + ((ks >> 1) & 1)];
+            if (ks & 1) w >>= 8;
+            const uint32_t b0 = (w & 0x000F000Fu) | 0x64006400u, b1 = (w & 0x00F000F0u) | 0x64006400u;
+            if (kk == 0) mma_f16_c(dacc[q], a, b0, b1, i0, i1); else mma_f16(dacc[q], a, b0, b1);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = cb * 32 + 8 * q + 2 * tq;
+          const uint32_t sp = *reinterpret_cast<const uint32_t *>(sh.ssc + gi * D + j);
+          const float2 s2 = make_float2(bf16_lo(sp), bf16_hi(sp));
+          float2 t0 = make_float2(dacc[q][0], dacc[q][1]), t1 = make_float2(dacc[q][2], dacc[q][3]);
+          if (ZP) {
+            const uint32_t zw = *reinterpret_cast<const uint16_t *>(sh.szp + gi * D + j);
+            const float2 z2 = make_float2((float)(zw & 0xFFu), (float)(zw >> 8));
+            t0 = __ffma2_rn(z2, make_float2(-c0.y, -c0.y), t0);
+            t1 = __ffma2_rn(z2, make_float2(-c1.y, -c1.y), t1);
+          }
+          if (gi == 0) {
+            pacc2[q][0] = __fmul2_rn(s2, t0);
+            pacc2[q][1] = __fmul2_rn(s2, t1);
+          } else {
+            pacc2[q][0] = __ffma2_rn(s2, t0, pacc2[q][0]);
+            pacc2[q][1] = __ffma2_rn(s2, t1, pacc2[q][1]);
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        if (v0 < nv) *reinterpret_cast<float2 *>(sh.pb + v0 * PB_STRIDE + 8 * n + 2 * tq) = pacc2[n][0];
+        if (v0 + 8 < nv) *reinterpret_cast<float2 *>(sh.pb + (v0 + 8) * PB_STRIDE + 8 * n + 2 * tq) = pacc2[n][1];
+      }
+    } else {
     float pacc[4][4];
 #pragma unroll
     for (int nh = 0; nh < NH; ++nh)          // int8 heads: two passes of two n-tiles (register budget)
@@ -622,6 +690,7 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
       if (v0 < nv) *reinterpret_cast<float2 *>(sh.pb + v0 * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][0], pacc[n][1]);
       if (v0 + 8 < nv)
         *reinterpret_cast<float2 *>(sh.pb + (v0 + 8) * PB_STRIDE + 8 * n + 2 * tq) = make_float2(pacc[n][2], pacc[n][3]);
+    }
     }
   }
   // without a flush the block's words are done with: the next block's load overlaps the replay
@@ -787,6 +856,10 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
             uint32_t pair;
             if (!zpm) {
               pair = __byte_perm(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410);   // bytes 1, 3 are 0
+              if (BITS == 4) {                 // each half is code + 8 in 1..15: no other bit is set
+                w0 = rr == 0 ? pair : w0 + (pair << (4 * rr));
+                continue;
+              }
             } else {
               const int c0 = min(max((int)(__float_as_uint(y.x) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
               const int c1 = min(max((int)(__float_as_uint(y.y) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
@@ -816,14 +889,14 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
             make_uint4(cw[pl][m][pp][0], cw[pl][m][pp][1], cw[pl][m][pp][2], cw[pl][m][pp][3]);
 }
 
-template <int D, int G, int BITS>
+template <int D, int G, int BITS, int ZP, int MX>
 __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
                         const MmaShared &sh) {
   constexpr int NG = D / G, NPP = D / 64, PL = BITS / 4;
   constexpr uint32_t PLANE = D * D / 8; // words per nibble plane
   const int lane = threadIdx.x & 31;
   const int dP = st.dP;
-  const int zpm = st.zero_point;
+  constexpr int zpm = ZP;
   uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
                               : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
   __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
@@ -835,7 +908,7 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   uint32_t cw[PL][2][NPP][4];
   dm_load_block<D, PL>(codes, 0, lane, cw);
   TokenIn<D / 32> tin;
-  dm_issue<D, G>(st, io, unit, has_token, sh, tin);
+  dm_issue<D, G, ZP, MX>(st, io, unit, has_token, sh, tin);
   const int m0 = st.m[unit];
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
     cp_async_wait_all();                         // nothing may land in shared memory after the warp leaves
@@ -848,13 +921,13 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   const int nv = mt + (has_token ? 3 : 0);
   const int dpp = dm_dpp(dP);
   float bt, sv;
-  dm_stage<D, G>(st, unit, m0, has_token, tin, sh, bt, sv);
+  dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh, bt, sv);
   dm_tables<D, G>(sh, nv, mt, dP, dpp, has_token, do_flush, bt, sv);
 
 #pragma unroll 1
   for (int cb = 0; cb < D / 32; ++cb) {
     if (cb > 0 && do_flush) dm_load_block<D, PL>(codes, cb, lane, cw);
-    dm_block<D, G, BITS>(st, io, unit, cb, m0, has_token, codes, scale, zpt, sh, cw, true);
+    dm_block<D, G, BITS, ZP, MX>(st, io, unit, cb, m0, has_token, codes, scale, zpt, sh, cw, true);
   }
   __syncwarp();
   if (lane == 0) st.m[unit] = do_flush ? 0 : mt;
@@ -863,8 +936,8 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 // One launch per code pool (int4 heads, int8 heads), so that each path gets its own register allocation
 // (int4: 16 warps per SM at <= 128 registers; int8, with twice the code words live: 12 warps per SM).
 // Warp w of the launch handles pool unit w: sequence w / HP, the pool's head slot w % HP.
-template <int D, int G, int BITS>
-__global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+template <int D, int G, int BITS, int ZP, int MX>
+__global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? PACE_DM_MIN_BLOCKS : 3) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int HP = BITS == 4 ? st.H4 : st.H8;
@@ -872,15 +945,15 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_mma_k
   if (w >= st.B * HP) return;
   const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
-  const MmaSmem L = mma_smem(D, G, st.dP, st.buf_mode == PACE_BUF_MIXED, st.zero_point);
+  const MmaSmem L = mma_smem(D, G, st.dP, MX, ZP);
   const MmaShared sh = mma_shared(smem + (size_t)warp * L.total, L, st.dP);
-  dm_unit<D, G, BITS>(st, io, b, h, b * st.H + h, has_token, sh);
+  dm_unit<D, G, BITS, ZP, MX>(st, io, b, h, b * st.H + h, has_token, sh);
 }
 
 // Few units in flight: one CTA per unit. Warp 0 stages the unit and builds its tables in the first work area,
 // then warp w runs column block w with its own dot and replay tables, so a unit's blocks run side by side and
 // the chain of dependent work per unit (the launch time at small batch) is about halved.
-template <int D, int G, int BITS>
+template <int D, int G, int BITS, int ZP, int MX>
 __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NG = D / G, NPP = D / 64, PL = BITS / 4, NB = D / 32;
@@ -892,8 +965,8 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split
   const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
   const int unit = b * st.H + h;
   const int dP = st.dP;
-  const int zpm = st.zero_point;
-  const MmaSmem L = mma_smem(D, G, dP, st.buf_mode == PACE_BUF_MIXED, zpm);
+  constexpr int zpm = ZP;
+  const MmaSmem L = mma_smem(D, G, dP, MX, zpm);
   const MmaShared sh0 = mma_shared(smem, L, dP);
   MmaShared shw = sh0;
   {
@@ -909,7 +982,7 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split
   uint32_t cw[PL][2][NPP][4];
   if (active) dm_load_block<D, PL>(codes, warp, lane, cw);
   TokenIn<D / 32> tin{};
-  if (warp == 0) dm_issue<D, G>(st, io, unit, has_token, sh0, tin, dP);
+  if (warp == 0) dm_issue<D, G, ZP, MX>(st, io, unit, has_token, sh0, tin, dP);
   const int m0 = st.m[unit];
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
     if (warp == 0) {
@@ -923,11 +996,11 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split
   const int do_flush = !has_token || mt == dP;
   if (warp == 0) {
     float bt, sv;
-    dm_stage<D, G>(st, unit, m0, has_token, tin, sh0, bt, sv);
+    dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh0, bt, sv);
     dm_tables<D, G>(sh0, mt + (has_token ? 3 : 0), mt, dP, dm_dpp(dP), has_token, do_flush, bt, sv);
   }
   __syncthreads();
-  if (active) dm_block<D, G, BITS>(st, io, unit, warp, m0, has_token, codes, scale, zpt, shw, cw, false);
+  if (active) dm_block<D, G, BITS, ZP, MX>(st, io, unit, warp, m0, has_token, codes, scale, zpt, shw, cw, false);
   __syncthreads();
   if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
 }
@@ -942,13 +1015,13 @@ static int dm_sm_count() {
   return sms;
 }
 
-template <int D, int G, int BITS>
+template <int D, int G, int BITS, int ZP, int MX>
 static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, size_t smem) {
   static size_t opted = 0;
   if (smem > 48 * 1024 && smem > opted) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_split_kernel<D, G, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      e = cudaFuncSetAttribute(decode_split_kernel<D, G, BITS, ZP, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     opted = 227 * 1024;
   }
@@ -956,28 +1029,35 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
   if (units == 0) return cudaSuccess;
   // one warp per unit while every SM holds 16 units' warps or more; below that, a CTA per unit
   if (units * DM_WARPS <= (long)dm_sm_count() * 16) {
-    decode_split_kernel<D, G, BITS><<<(unsigned)units, DM_WARPS * 32, smem, s>>>(d, io, has_token);
+    decode_split_kernel<D, G, BITS, ZP, MX><<<(unsigned)units, DM_WARPS * 32, smem, s>>>(d, io, has_token);
   } else {
     const long blocks = (units + DM_WARPS - 1) / DM_WARPS;
-    decode_mma_kernel<D, G, BITS><<<(unsigned)blocks, DM_WARPS * 32, smem, s>>>(d, io, has_token);
+    decode_mma_kernel<D, G, BITS, ZP, MX><<<(unsigned)blocks, DM_WARPS * 32, smem, s>>>(d, io, has_token);
   }
   return cudaGetLastError();
 }
 
-template <int D, int G>
+template <int D, int G, int ZP, int MX>
 static cudaError_t launch_mma_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  const MmaSmem L = mma_smem(D, G, d.dP, d.buf_mode == PACE_BUF_MIXED, d.zero_point);
+  const MmaSmem L = mma_smem(D, G, d.dP, MX, ZP);
   const size_t smem = (size_t)DM_WARPS * L.total;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pool<D, G, 4>(d, io, has_token, s, smem);
-  if (e == cudaSuccess) e = launch_pool<D, G, 8>(d, io, has_token, s, smem);
+  cudaError_t e = launch_pool<D, G, 4, ZP, MX>(d, io, has_token, s, smem);
+  if (e == cudaSuccess) e = launch_pool<D, G, 8, ZP, MX>(d, io, has_token, s, smem);
   return e;
 }
 
-}  // namespace pace
-
-cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  using namespace pace;
-  if (d.D == 128) return d.G == 64 ? launch_mma_t<128, 64>(d, io, has_token, s) : launch_mma_t<128, 32>(d, io, has_token, s);
-  return d.G == 64 ? launch_mma_t<64, 64>(d, io, has_token, s) : launch_mma_t<64, 32>(d, io, has_token, s);
+// Every (D, G) of one zero-point mode and buffer format; each combination is instantiated in a translation
+// unit of its own so that they compile in parallel.
+template <int ZP, int MX>
+cudaError_t launch_quant_zm(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  if (d.D == 128)
+    return d.G == 64 ? launch_mma_t<128, 64, ZP, MX>(d, io, has_token, s) : launch_mma_t<128, 32, ZP, MX>(d, io, has_token, s);
+  return d.G == 64 ? launch_mma_t<64, 64, ZP, MX>(d, io, has_token, s) : launch_mma_t<64, 32, ZP, MX>(d, io, has_token, s);
 }
+extern template cudaError_t launch_quant_zm<0, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_quant_zm<0, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_quant_zm<1, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_quant_zm<1, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+
+}  // namespace pace

@@ -277,7 +277,7 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
     if (e != cudaSuccess) return cuda_fail(e, "prefill flush launch");
   }
   PaceIO io{q, k, v, a, beta, o, n_tokens};
-  e = pace_launch_prefill(state->dev, io, cs);
+  e = pace_prefill_tc_supported(state->dev) ? pace_launch_prefill_tc(state->dev, io, cs) : pace_launch_prefill(state->dev, io, cs);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ok();
 }

@@ -49,6 +49,9 @@ cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token
 cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
+// Tensor-core chunk prefill (d_k = d_v = 128, bf16 I/O); pace_prefill_tc_supported says whether it applies.
+bool pace_prefill_tc_supported(const PaceDev &d);
+cudaError_t pace_launch_prefill_tc(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s);
 cudaError_t pace_launch_dequantize_state(const PaceDev &d, float *S, cudaStream_t s);
 cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, float *e_out,
