@@ -33,6 +33,9 @@
 namespace pace {
 
 constexpr int DM_WARPS = 4;   // units (warps) per block
+#ifndef PACE_DM_CTA_PER_UNIT
+#define PACE_DM_CTA_PER_UNIT 0  // 1: the CTA-per-unit kernel at every batch size
+#endif
 #ifndef PACE_DM_MIN_BLOCKS
 #define PACE_DM_MIN_BLOCKS 4  // resident blocks per SM the int4 kernels are compiled for (register cap)
 #endif
@@ -950,9 +953,287 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? PACE_DM_MIN_BLOCKS 
   dm_unit<D, G, BITS, ZP, MX>(st, io, b, h, b * st.H + h, has_token, sh);
 }
 
-// Few units in flight: one CTA per unit. Warp 0 stages the unit and builds its tables in the first work area,
-// then warp w runs column block w with its own dot and replay tables, so a unit's blocks run side by side and
-// the chain of dependent work per unit (the launch time at small batch) is about halved.
+// ---- cooperative form: the four warps of a CTA stage one unit together ---------------------------------------
+// Named barrier among the CTA's warps (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void dc_bar() { asm volatile("bar.sync 1, %0;" ::"r"(DM_WARPS * 32) : "memory"); }
+
+// Loads that do not depend on the buffer count, split by role: warp 0 the key side (new k and q, every buffered
+// key row, the per-token scalars), warp 1 the value side (new v, every buffered value row), warp 3 the per-token
+// scalars; the group scales and zero points by all four. Every buffered row is fetched before the count is known
+// (at most dP rows), so the count read and the row copies are in flight together. The q digit rows share the
+// key-row area with those copies, so the warp that issues the copies also writes the digits, after its wait.
+template <int D, int G, int ZP, int MX>
+__device__ __forceinline__ void dc_issue(const PaceDev &st, const PaceIO &io, int unit, int has_token, const MmaShared &sh,
+                                         int warp, float (&x)[D / 32], float (&xq)[D / 32], float4 &bs, float &an,
+                                         float &bn) {
+  constexpr int CPL = D / 32, NG = D / G;
+  const int lane = threadIdx.x & 31, dP = st.dP, tid = threadIdx.x;
+  const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
+  for (int c = tid; c < NG * D * 2 / 16; c += DM_WARPS * 32) cp_async16(reinterpret_cast<char *>(sh.ssc) + 16 * c, gs + 16 * c);
+  if (ZP) {
+    const char *gz = reinterpret_cast<const char *>(st.zp + (size_t)unit * NG * D);
+    for (int c = tid; c < NG * D / 16; c += DM_WARPS * 32) cp_async16(sh.szp + 16 * c, gz + 16 * c);
+  }
+  const int rk = MX ? D / 2 : D, rv = MX ? 2 * D : D;
+  if (warp == 0) {
+    unsigned char *kdst = MX ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
+    const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
+    for (int c = lane; c < dP * rk / 16; c += 32) cp_async16(kdst + 16 * c, gk + 16 * c);
+  } else if (warp == 1) {
+    const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
+    for (int c = lane; c < dP * rv / 16; c += 32) cp_async16(sh.vrow + 16 * c, gv + 16 * c);
+  }
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) x[c] = xq[c] = 0.0f;
+  an = bn = 0.0f;
+  bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (has_token) {
+    const size_t e0 = (size_t)unit * D + CPL * lane;
+    if (warp < 2) dm_load_io<CPL>(warp == 0 ? io.k : io.v, e0, st.io, x);
+    if (warp == 0) dm_load_io<CPL>(io.q, e0, st.io, xq);
+    an = io.a[unit];
+    bn = io.beta[unit];
+  }
+  if ((warp == 0 || warp == 3) && lane < dP) bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
+}
+
+// Stage the new token and the tables that need no MMA, by role (see dc_issue). Leaves in shared memory what the
+// single-warp staging leaves, plus beta_t (bet) and the value scales s_vt (svt).
+template <int D, int G, int MX>
+__device__ void dc_stage(const PaceDev &st, int unit, int m0, int has_token, const MmaShared &sh, int warp,
+                         const float (&x)[D / 32], const float (&xq)[D / 32], float4 bs, float an, float bn) {
+  constexpr int CPL = D / 32;
+  const int lane = threadIdx.x & 31, col0 = CPL * lane, dP = st.dP, mt = m0 + has_token;
+  cp_async_wait_all();
+  __syncwarp();
+  if (warp == 0) {                                      // key side
+    if (MX) {
+      const unsigned char *kp = reinterpret_cast<const unsigned char *>(sh.ah);
+      for (int t = 0; t < m0; ++t) {
+        if (lane < D / 8) {                             // one 8-key run per lane: nibble code + 8 -> int8
+          const uint32_t nb = *reinterpret_cast<const uint32_t *>(kp + t * (D / 2) + 4 * lane);
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            lo |= (uint32_t)(((int)((nb >> (8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
+            hi |= (uint32_t)(((int)((nb >> (16 + 8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
+          }
+          *reinterpret_cast<uint2 *>(sh.krow + t * D + 8 * lane) = make_uint2(lo, hi);
+        }
+      }
+    }
+    float sk = 0.0f;
+    if (has_token) {
+      float mk = 0.0f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) mk = fmaxf(mk, fabsf(x[c]));
+      const float Ak = warp_max(mk);
+      const int qk = MX ? 7 : 127;
+      const bool kz = !(Ak >= FLT_MIN);
+      const float rkk = kz ? 0.0f : __fdiv_rn((float)qk, Ak);
+      sk = kz ? 0.0f : __fdiv_rn(Ak, (float)qk);
+      int ck[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) ck[c] = min(max(__float2int_rn(__fmul_rn(x[c], rkk)), -qk), qk);
+      dm_store_bytes<CPL>(sh.krow + m0 * D + col0, ck);
+      if (MX) {
+        uint8_t *bk = static_cast<uint8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * (D / 2) + col0 / 2;
+#pragma unroll
+        for (int c = 0; c < CPL; c += 2) bk[c / 2] = (uint8_t)((ck[c] + 8) | ((ck[c + 1] + 8) << 4));
+      } else {
+        dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * D + col0, ck);
+      }
+      if (lane == 0) {
+        float *e = st.buf_s + ((size_t)unit * dP + m0) * 4;
+        *reinterpret_cast<float2 *>(e) = make_float2(an, bn);
+        e[2] = sk;
+      }
+    }
+    if (lane < mt) sh.vsc[lane] = lane < m0 ? bs.z : sk;
+    // q as three balanced base-256 digits
+    if (has_token) {
+      float mq = 0.0f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) mq = fmaxf(mq, fabsf(xq[c]));
+      const float Aq = warp_max(mq);
+      const float QMAX = 8323072.0f;
+      const bool qz = !(Aq >= FLT_MIN);
+      const float sigma = qz ? 0.0f : __fdiv_rn(Aq, QMAX);
+      const float rq = qz ? 0.0f : __fdiv_rn(QMAX, Aq);
+      int d2[CPL], d1[CPL], d0[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int qi = min(max(__float2int_rn(xq[c] * rq), -8323072), 8323072);
+        const int q1 = (qi + 128) >> 8;
+        d0[c] = qi - (q1 << 8);
+        d2[c] = (q1 + 128) >> 8;
+        d1[c] = q1 - (d2[c] << 8);
+      }
+      dm_store_bytes<CPL>(sh.krow + mt * D + col0, d2);
+      dm_store_bytes<CPL>(sh.krow + (mt + 1) * D + col0, d1);
+      dm_store_bytes<CPL>(sh.krow + (mt + 2) * D + col0, d0);
+      if (lane == 0) {
+        sh.vsc[mt] = 65536.0f * sigma;
+        sh.vsc[mt + 1] = 256.0f * sigma;
+        sh.vsc[mt + 2] = sigma;
+      }
+    }
+  } else if (warp == 1) {                               // value side
+    float sv = 0.0f;
+    if (has_token) {
+      if (MX) {
+        __nv_bfloat16 *bv = static_cast<__nv_bfloat16 *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0;
+        uint32_t *vr = reinterpret_cast<uint32_t *>(sh.vrow + ((size_t)m0 * D + col0) * 2);
+#pragma unroll
+        for (int c = 0; c < CPL; c += 2) {
+          const __nv_bfloat162 pv = __floats2bfloat162_rn(x[c], x[c + 1]);
+          *reinterpret_cast<__nv_bfloat162 *>(bv + c) = pv;
+          vr[c / 2] = *reinterpret_cast<const uint32_t *>(&pv);
+        }
+      } else {
+        float mv = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) mv = fmaxf(mv, fabsf(x[c]));
+        const float Av = warp_max(mv);
+        const bool vz = !(Av >= FLT_MIN);
+        const float rvv = vz ? 0.0f : __fdiv_rn(127.0f, Av);
+        sv = vz ? 0.0f : __fdiv_rn(Av, 127.0f);
+        int cv[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) cv[c] = min(max(__float2int_rn(__fmul_rn(x[c], rvv)), -127), 127);
+        dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0, cv);
+        dm_store_bytes<CPL>(sh.vrow + m0 * D + col0, cv);
+      }
+      if (lane == 0) st.buf_s[((size_t)unit * dP + m0) * 4 + 3] = sv;
+    }
+    // value scales of the buffered tokens: read back from global (written by the earlier steps)
+    if (lane < m0) sh.svt[lane] = st.buf_s[((size_t)unit * dP + lane) * 4 + 3];
+    if (lane == m0 && has_token) sh.svt[lane] = sv;
+  } else if (warp == 3) {                              // decays: G_t, G_m/G_t and the ratios G_t/G_s
+    if (lane < mt) {
+      sh.a[lane] = lane < m0 ? bs.x : an;
+      sh.bet[lane] = lane < m0 ? bs.y : bn;
+    }
+    __syncwarp();
+    if (lane < mt) {
+      const int ws = dm_wstride(dP);
+      float g = 1.0f, dm = 1.0f;
+      for (int r = 0; r <= lane; ++r) g *= sh.a[r];
+      for (int r = lane + 1; r < mt; ++r) dm *= sh.a[r];
+      sh.gam[lane] = g;
+      sh.dmq[lane] = dm;
+      float p = 1.0f;                                   // G_t/G_s = a_{s+1} .. a_t for t = lane, s < t
+      for (int s2 = lane - 1; s2 >= 0; --s2) {
+        p *= sh.a[s2 + 1];
+        sh.dmt[lane * ws + s2] = p;
+      }
+    }
+  }
+}
+
+// The fp16 rows of the vectors (rows >= nv zero; keys 8..15 of every 16-key step scaled by 1/16) and, for a
+// flush, the bf16 key table kbf[i][s]: split over the CTA's threads.
+template <int D>
+__device__ void dc_rows(const MmaShared &sh, int nv, int mt, int dpp, int do_flush) {
+  const int tid = threadIdx.x;
+  const int nvt = (nv + 15) >> 4;
+  for (int idx = tid; idx < 16 * nvt * (D / 8); idx += DM_WARPS * 32) {
+    const int row = idx / (D / 8), k8 = 8 * (idx - row * (D / 8));
+    uint4 h = make_uint4(0u, 0u, 0u, 0u);
+    if (row < nv) {
+      const uint2 x = *reinterpret_cast<const uint2 *>(sh.krow + row * D + k8);
+      const bool sx = (k8 & 8) != 0;
+      h = make_uint4(i8pair_f16(x.x, 0x4140, sx), i8pair_f16(x.x, 0x4342, sx), i8pair_f16(x.y, 0x4140, sx),
+                     i8pair_f16(x.y, 0x4342, sx));
+    }
+    *reinterpret_cast<uint4 *>(sh.ah + ah_off<D>(row, k8 >> 3)) = h;
+  }
+  if (do_flush) {
+    const int half = dpp >> 1;
+    for (int idx = tid; idx < D * half; idx += DM_WARPS * 32) {
+      const int i = idx / half, s2 = 2 * (idx - i * half);
+      const float k0 = s2 < mt ? (float)sh.krow[s2 * D + i] : 0.0f;
+      const float k1 = s2 + 1 < mt ? (float)sh.krow[(s2 + 1) * D + i] : 0.0f;
+      sh.kbf[idx] = bf16x2_bits(k0, k1);
+    }
+  }
+}
+
+// Tables by MMA of the fp16 rows, split over two warps: warp 0 the group sums (T1, T2), warp 1 the Gram
+// coefficients W and the digit products k_s.q, then the per-token replay table tk and the flush coefficients ck.
+template <int D, int G>
+__device__ void dc_tables(const MmaShared &sh, int nv, int mt, int dP, int has_token, int warp) {
+  constexpr int KS = D / 16, KSG = G / 16, NG = D / G;
+  const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
+  const int nvt = (nv + 15) >> 4;
+  const int ws = dm_wstride(dP);
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;
+  const int brow = lane & 7, bcol = (lane >> 3) & 1;
+  if (warp == 0) {
+    for (int vt = 0; vt < nvt; ++vt) {
+      float cs[4];
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, sh.ah + ah_off<D>(16 * vt + arow, 2 * ks + acol));
+        const int gi = ks / KSG;                        // sums: column 2gi (first halves), 2gi + 1 (second halves)
+        const uint32_t o0 = g8 == 2 * gi ? 0x3C003C00u : 0u, o1 = g8 == 2 * gi + 1 ? 0x3C003C00u : 0u;
+        if (ks == 0) mma_f16_z(cs, a, o0, o1); else mma_f16(cs, a, o0, o1);
+      }
+      const int v0 = 16 * vt + g8;
+      if (tq < NG) {
+        sh.cf[v0 * 4 + tq] = make_float2(1024.0f * (cs[0] + cs[1]), cs[0] + 16.0f * cs[1]);
+        sh.cf[(v0 + 8) * 4 + tq] = make_float2(1024.0f * (cs[2] + cs[3]), cs[2] + 16.0f * cs[3]);
+      }
+    }
+  } else if (warp == 1) {
+    const int ntg = (mt + 7) >> 3;                      // 8-token tiles of the Gram columns
+    for (int vt = 0; vt < nvt; ++vt) {
+      float gr[4][4];
+#pragma unroll 2
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(a, sh.ah + ah_off<D>(16 * vt + arow, 2 * ks + acol));
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          if (n < ntg) {
+            uint32_t bb[2];
+            ldsm_x2(bb, sh.ah + ah_off<D>(8 * n + brow, 2 * ks + bcol));
+            const uint32_t b1 = f16x2_scale(bb[1], 256.0f);
+            if (ks == 0) mma_f16_z(gr[n], a, bb[0], b1); else mma_f16(gr[n], a, bb[0], b1);
+          }
+        }
+      }
+      const int v0 = 16 * vt + g8;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        if (n >= ntg) continue;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = v0 + 8 * (e >> 1), s2 = 8 * n + 2 * tq + (e & 1);
+          if (s2 >= mt) continue;
+          if (v < mt && s2 < v)
+            sh.W[v * ws + s2] = sh.dmt[v * ws + s2] * sh.vsc[s2] * sh.vsc[v] * gr[n][e];
+          else if (v >= mt && v < nv)
+            sh.e3[(v - mt) * dP + s2] = gr[n][e];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane < mt) {
+      const float dv = sh.dmq[lane] * sh.vsc[lane];
+      const float cq = has_token ? dv * (sh.vsc[mt] * sh.e3[lane] + (sh.vsc[mt + 1] * sh.e3[dP + lane] +
+                                                                     sh.vsc[mt + 2] * sh.e3[2 * dP + lane]))
+                                 : 0.0f;
+      sh.ck[lane] = dv;
+      sh.tk[lane] = make_float4(sh.gam[lane] * sh.vsc[lane], sh.bet[lane], sh.svt[lane], cq);
+    }
+  }
+}
+
+// One CTA per unit. The four warps stage the unit and build its tables together (dc_issue, dc_stage, dc_rows,
+// dc_tables, three barriers), in the first work area; then warp w runs column block w with its own dot and
+// replay tables. The chain of dependent work per warp is about a quarter of the one-warp-per-unit kernel's.
 template <int D, int G, int BITS, int ZP, int MX>
 __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -981,25 +1262,25 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split
   const bool active = warp < NB;
   uint32_t cw[PL][2][NPP][4];
   if (active) dm_load_block<D, PL>(codes, warp, lane, cw);
-  TokenIn<D / 32> tin{};
-  if (warp == 0) dm_issue<D, G, ZP, MX>(st, io, unit, has_token, sh0, tin, dP);
+  float x[D / 32], xq[D / 32], an, bn;
+  float4 bs;
+  dc_issue<D, G, ZP, MX>(st, io, unit, has_token, sh0, warp, x, xq, bs, an, bn);
   const int m0 = st.m[unit];
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
-    if (warp == 0) {
-      cp_async_wait_all();                       // nothing may land in shared memory after the CTA leaves
-      if (has_token && m0 != 0)                  // corrupted counter: leave the unit, emit zeros
-        for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
-    }
+    cp_async_wait_all();                         // nothing may land in shared memory after the CTA leaves
+    if (warp == 0 && has_token && m0 != 0)       // corrupted counter: leave the unit, emit zeros
+      for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
     return;
   }
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
-  if (warp == 0) {
-    float bt, sv;
-    dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh0, bt, sv);
-    dm_tables<D, G>(sh0, mt + (has_token ? 3 : 0), mt, dP, dm_dpp(dP), has_token, do_flush, bt, sv);
-  }
-  __syncthreads();
+  const int nv = mt + (has_token ? 3 : 0);
+  dc_stage<D, G, MX>(st, unit, m0, has_token, sh0, warp, x, xq, bs, an, bn);
+  dc_bar();
+  dc_rows<D>(sh0, nv, mt, dm_dpp(dP), do_flush);
+  dc_bar();
+  dc_tables<D, G>(sh0, nv, mt, dP, has_token, warp);
+  dc_bar();
   if (active) dm_block<D, G, BITS, ZP, MX>(st, io, unit, warp, m0, has_token, codes, scale, zpt, shw, cw, false);
   __syncthreads();
   if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
@@ -1028,7 +1309,7 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
   const long units = (long)d.B * (BITS == 4 ? d.H4 : d.H8);
   if (units == 0) return cudaSuccess;
   // one warp per unit while every SM holds 16 units' warps or more; below that, a CTA per unit
-  if (units * DM_WARPS <= (long)dm_sm_count() * 16) {
+  if (PACE_DM_CTA_PER_UNIT || units * DM_WARPS <= (long)dm_sm_count() * 16) {
     decode_split_kernel<D, G, BITS, ZP, MX><<<(unsigned)units, DM_WARPS * 32, smem, s>>>(d, io, has_token);
   } else {
     const long blocks = (units + DM_WARPS - 1) / DM_WARPS;
