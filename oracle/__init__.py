@@ -20,7 +20,7 @@ _SRC = os.path.join(_HERE, "pace_oracle.c")
 _SO = os.path.join(_HERE, "liboracle.so")
 
 BUF_INT8, BUF_MIXED, BUF_FP32 = 0, 1, 2
-STATE_QUANT, STATE_FP32, STATE_BF16 = 0, 1, 2
+STATE_QUANT, STATE_FP32, STATE_BF16, STATE_BF16_BUF = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:

@@ -199,7 +199,7 @@ static void load_state(const orc_cfg *cfg, const orc_unit *u, double *S) {
 }
 
 /* Round the working state once and store it: quantized mode rounds the fp32 image with the       */
-/* key-axis quantizer; fp32 (test) mode keeps it exact; bf16 mode stores bf16(fp32(S)).           */
+/* key-axis quantizer; fp32 (test) mode keeps it exact; both bf16 modes store bf16(fp32(S)).      */
 static void store_state(const orc_cfg *cfg, orc_unit *u, const double *S) {
   const long n = (long)cfg->d_k * cfg->d_v;
   if (cfg->state_mode == ORC_STATE_QUANT) {
@@ -207,7 +207,7 @@ static void store_state(const orc_cfg *cfg, orc_unit *u, const double *S) {
     for (long e = 0; e < n; ++e) S32[e] = (float)S[e];
     orc_quantize_state(cfg, S32, u->code, u->scale, u->zp);
     free(S32);
-  } else if (cfg->state_mode == ORC_STATE_BF16) {
+  } else if (cfg->state_mode == ORC_STATE_BF16 || cfg->state_mode == ORC_STATE_BF16_BUF) {
     for (long e = 0; e < n; ++e) u->S[e] = (double)orc_bf16_rn((float)S[e]);
   } else {
     memcpy(u->S, S, sizeof(double) * n);
@@ -262,7 +262,9 @@ static void replay(const orc_cfg *cfg, const orc_unit *u, double *S) {
 /* One decode step ([P1] 어떻게 동작하나: the state is rounded once per dP generated tokens; the     */
 /* buffered tokens are applied to the state all at once at the flush). Per-token bf16 mode is the  */
 /* pages' comparison point ([P1] 전제와 한계, throughput study): no buffer, bf16 state every token;  */
-/* the output is read from the state before it is rounded, as in the PACE path.                    */
+/* the output is read from the state before it is rounded, as in the PACE path. Buffered bf16 mode */
+/* ([P1] 전제와 한계: most of the TPOT gain comes from the decode buffer with a bf16 state) takes    */
+/* the PACE path below with bf16 rounding in place of the key-axis quantizer.                      */
 void orc_decode_step(const orc_cfg *cfg, orc_unit *u, const float *q, const float *k, const float *v, float a,
                      float beta, double *o) {
   const int dk = cfg->d_k, dv = cfg->d_v;

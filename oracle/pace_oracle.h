@@ -25,7 +25,9 @@ extern "C" {
 #endif
 
 enum { ORC_BUF_INT8 = 0, ORC_BUF_MIXED = 1, ORC_BUF_FP32 = 2 };
-enum { ORC_STATE_QUANT = 0, ORC_STATE_FP32 = 1, ORC_STATE_BF16 = 2 };
+/* ORC_STATE_BF16: per-token bf16 state, no buffer (the pages' comparison point).
+ * ORC_STATE_BF16_BUF: bf16 state with PACE's decode buffer: rounded to bf16 once every dP tokens. */
+enum { ORC_STATE_QUANT = 0, ORC_STATE_FP32 = 1, ORC_STATE_BF16 = 2, ORC_STATE_BF16_BUF = 3 };
 
 typedef struct {
   int d_k, d_v;
@@ -42,7 +44,7 @@ typedef struct {
   int32_t *code;   /* [d_k*d_v]          quantized mode */
   float   *scale;  /* [(d_k/g)*d_v]      quantized mode */
   int32_t *zp;     /* [(d_k/g)*d_v]      quantized mode, zero-point only */
-  double  *S;      /* [d_k*d_v]          fp32 mode (kept exact, fp64) and bf16 mode (bf16 values) */
+  double  *S;      /* [d_k*d_v]          fp32 mode (kept exact, fp64); bf16 modes (bf16 values) */
   int      m;      /* tokens held in the decode buffer */
   /* decode buffer, dP slots */
   int32_t *bk;     /* [dP*d_k] key codes (int8 or int4 mode) */

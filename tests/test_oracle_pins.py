@@ -352,6 +352,55 @@ def test_current_token_enters_its_output_through_buffered_values():
     assert not np.allclose(o, float(tk["beta"]) * (tk["k"] @ tk["q"]) * tk["v"], rtol=1e-6)
 
 
+@pytest.mark.parametrize("buf", [O.BUF_INT8, O.BUF_MIXED])
+def test_buffered_bf16_state_rounds_once_per_period(buf):
+    """Buffered bf16 mode: between roundings the outputs are the plain fp64 recurrence of the buffered
+    (quantized) tokens from the last rounded state; every dP-th step the state becomes torch's bf16 rounding
+    of that recurrence, and nothing else changes it."""
+    import torch
+    dk, dv, dP = 32, 16, 4
+    cfg = O.Cfg(d_k=dk, d_v=dv, g=32, dP=dP, buf_mode=buf, state_mode=O.STATE_BF16_BUF)
+    unit = O.Unit(cfg)
+    S0 = torch.from_numpy(RNG.standard_normal((dk, dv)).astype(np.float32)).to(torch.bfloat16).double().numpy()
+    unit.S[...] = S0
+    S = S0.copy()
+    for t, tk in enumerate(_tokens(3 * dP + 2, dk, dv)):
+        before = unit.S.copy()
+        o = O.decode_step(unit, tk["q"], tk["k"], tk["v"], tk["a"], tk["beta"])
+        if buf == O.BUF_MIXED:
+            kc, sk = O.buffer_quant(tk["k"], 7)
+            vd = O.bf16_rn(tk["v"]).astype(np.float64)
+        else:
+            kc, sk = O.buffer_quant(tk["k"], 127)
+            vc, sv = O.buffer_quant(tk["v"], 127)
+            vd = float(sv) * vc.astype(np.float64)
+        O.token_update(S, float(sk) * kc.astype(np.float64), vd, float(tk["a"]), float(tk["beta"]))
+        np.testing.assert_allclose(o, S.T @ tk["q"].astype(np.float64), rtol=1e-12, atol=1e-12)
+        if (t + 1) % dP == 0:
+            S = torch.from_numpy(S.astype(np.float32)).to(torch.bfloat16).double().numpy()
+            assert np.array_equal(unit.S, S) and unit.m == 0
+        else:
+            assert np.array_equal(unit.S, before) and unit.m == (t + 1) % dP
+    O.flush(unit)
+    S = torch.from_numpy(S.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert unit.m == 0 and np.array_equal(unit.S, S)
+
+
+def test_buffered_bf16_with_period_one_and_exact_buffer_is_the_per_token_mode():
+    """dP = 1 with an unquantized buffer rounds after every token: the same trajectory as the per-token
+    bf16 comparison mode, bit for bit."""
+    dk, dv = 16, 8
+    a = O.Unit(O.Cfg(d_k=dk, d_v=dv, g=16, dP=1, buf_mode=O.BUF_FP32, state_mode=O.STATE_BF16_BUF))
+    b = O.Unit(O.Cfg(d_k=dk, d_v=dv, g=16, dP=1, buf_mode=O.BUF_FP32, state_mode=O.STATE_BF16))
+    S0 = O.bf16_rn(RNG.standard_normal((dk, dv))).astype(np.float64)
+    a.S[...] = S0
+    b.S[...] = S0
+    for tk in _tokens(12, dk, dv):
+        oa = O.decode_step(a, tk["q"], tk["k"], tk["v"], tk["a"], tk["beta"])
+        ob = O.decode_step(b, tk["q"], tk["k"], tk["v"], tk["a"], tk["beta"])
+        assert np.array_equal(oa, ob) and np.array_equal(a.S, b.S)
+
+
 def test_bf16_state_rounds_every_token():
     dk, dv = 16, 8
     cfg = O.Cfg(d_k=dk, d_v=dv, g=16, state_mode=O.STATE_BF16, buf_mode=O.BUF_FP32)
