@@ -129,6 +129,15 @@ def decode_bytes_period_avg(D, g, dP, **kw) -> float:
     return sum(decode_bytes_per_unit(D, g, dP, m0, **kw) for m0 in range(dP)) / dP
 
 
+def bf16buf_bytes_per_period_avg(D: int, dP: int) -> float:
+    """Buffered bf16 state, averaged over a period: the bf16 state read every step and written once per period,
+    plus the same buffer and token traffic as PACE-4 (int8 buffer)."""
+    entry = 2 * D + 16
+    io = 3 * D * 2 + D * 2 + 8
+    state = D * D * 2
+    return state + state / dP + sum(m0 * entry for m0 in range(dP)) / dP + entry + io + 8
+
+
 def bf16_bytes_per_unit(D: int) -> int:
     return 2 * D * D * 2 + 3 * D * 2 + D * 2 + 8
 
@@ -360,8 +369,9 @@ def rotation_count(nbytes: int, dP: int, align_dp: bool) -> int:
 def measure(P, torch, wl, state_mode, K, W, sampler=None, min_sets=2):
     bytes1 = P.pace_state_bytes(P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, state_mode=state_mode,
                                               buf_mode=P.PACE_BUF_INT8))
-    R = max(rotation_count(bytes1, wl.dP, state_mode == P.PACE_STATE_QUANT), min_sets)
-    if state_mode == P.PACE_STATE_QUANT:
+    periodic = state_mode in (P.PACE_STATE_QUANT, P.PACE_STATE_BF16_BUF)
+    R = max(rotation_count(bytes1, wl.dP, periodic), min_sets)
+    if periodic:
         R = -(-R // wl.dP) * wl.dP
     setup = DecodeSetup(P, torch, wl, state_mode, R)
     ms = time_steps(torch, setup, K, W, sampler)
@@ -371,13 +381,15 @@ def measure(P, torch, wl, state_mode, K, W, sampler=None, min_sets=2):
 def batch_sweep(P, torch, token_steps=100):
     """The pages' throughput study shape: 24 gated-delta layers x 16 heads, one token step = 24 sequential layer
     launches (each layer its own state set, in one CUDA graph); PACE-4 dP=8 against the per-token bf16 kernel at
-    every batch size. Returns per-batch tokens/s of both and the smallest batch from which PACE-4 stays faster."""
+    every batch size, with the buffered bf16 state (the decode buffer without the 4-bit state) beside them.
+    Returns per-batch tokens/s and the smallest batch from which PACE-4 stays faster than per-token bf16."""
     import synth
     out, L = {}, 24
     for b in (1, 2, 4, 8, 16, 32, 64, 128):
         wl = synth.workload("sweep", B=b)
         row = {}
-        for name, mode in (("pace4", P.PACE_STATE_QUANT), ("bf16", P.PACE_STATE_BF16)):
+        for name, mode in (("pace4", P.PACE_STATE_QUANT), ("bf16", P.PACE_STATE_BF16),
+                           ("bf16buf", P.PACE_STATE_BF16_BUF)):
             s, ms, R = measure(P, torch, wl, mode, token_steps * L, 3 * L, min_sets=L)
             row[f"{name}_tokens_per_s"] = b / (ms * L * 1e-3)
             row[f"{name}_ms_per_token_step"] = ms * L
@@ -393,6 +405,37 @@ def batch_sweep(P, torch, token_steps=100):
             break
     return {"layers": L, "heads": 16, "d": 128, "per_batch": out, "pace4_faster_from_batch": cross,
             "note": "one token step = 24 layer launches on distinct state sets; >= 24 sets rotate"}
+
+
+def prefill_longctx(P, torch, n_tokens=32768, distinct=8):
+    """Long-context prefill shaped like the pages' 32,768-token study: 48 heads, d=128, batch 16, PACE-4 g=64,
+    slow decay, n_tokens in 256-token chunks (the state rounded once per chunk). `distinct` chunks of inputs are
+    drawn on the device and reused cyclically (the state carries on); CUDA events time the chunk launches only.
+    FLOPs per unit and chunk are those of the tensor-core form (the dense contractions of the chunk kernel)."""
+    import synth
+    wl = synth.workload("longctx")
+    cfg = P.make_config(wl.H, wl.d_k, wl.B, dP=8, group=wl.g)
+    st = P.PaceState(cfg, wl.B)
+    chunks = [synth.device_chunk_inputs(wl, 256 * c, 256) for c in range(distinct)]
+    o = torch.empty(wl.B, wl.H, 256, wl.d_v, dtype=torch.bfloat16, device="cuda")
+    n_chunks = n_tokens // 256
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for c in range(n_chunks):
+        x = chunks[c % distinct]
+        st.prefill_chunk(x["q"], x["k"], x["v"], x["a"], x["beta"], o)
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1])
+    st.close()
+    units = wl.B * wl.H
+    # per 32-token sub-chunk: S^T [k|q] (2 parts, 128x64x128), Gram (128x32x128), update (2 parts, 128x128x32)
+    flop_sub = 2 * (2 * 128 * 64 * 128 + 128 * 32 * 128 + 2 * 128 * 128 * 32)
+    tflops = units * n_chunks * 8 * flop_sub / (ms * 1e-3) / 1e12
+    return {"B": wl.B, "H": wl.H, "d": wl.d_k, "tokens": n_tokens, "chunks": n_chunks, "ms": ms,
+            "tokens_per_s": wl.B * n_tokens / (ms * 1e-3), "tensor_tflops": tflops,
+            "note": "tensor-core chunk prefill; inputs drawn on the device, 8 distinct chunks reused"}
 
 
 def main():
@@ -452,6 +495,12 @@ def main():
             extra[f"bf16_pertoken_b{b}"] = {"tokens_per_s": b / (ms2 * 1e-3), "ms_per_step": ms2, "rotating_sets": R2,
                                             "achieved_gbs": b * wlb.H * bf16_bytes_per_unit(128) / (ms2 * 1e-3) / 1e9}
             s2.close()
+            s4, ms4, R4 = measure(P, torch, wlb, P.PACE_STATE_BF16_BUF, k2, max(3, W // 4))
+            extra[f"bf16_buffered_b{b}"] = {
+                "tokens_per_s": b / (ms4 * 1e-3), "ms_per_step": ms4, "rotating_sets": R4,
+                "achieved_gbs": b * wlb.H * bf16buf_bytes_per_period_avg(128, 8) / (ms4 * 1e-3) / 1e9,
+                "note": "bf16 state rounded once every dP=8 tokens, int8 decode buffer (no 4-bit state)"}
+            s4.close()
             if b == 128:
                 s3, ms3, R3 = measure(P, torch, wlb, P.PACE_STATE_QUANT, k2, max(3, W // 4))
                 alg3 = b * wlb.H * decode_bytes_period_avg(128, 64, 8)
@@ -461,6 +510,7 @@ def main():
                 s3.close()
             torch.cuda.empty_cache()
         extra["sweep_24x16"] = batch_sweep(P, torch)
+        extra["prefill_longctx"] = prefill_longctx(P, torch)
 
     cb = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:

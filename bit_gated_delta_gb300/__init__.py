@@ -11,7 +11,7 @@ import ctypes as C
 import numpy as np
 
 from ._lib import (PACE_BUF_FP32, PACE_BUF_INT8, PACE_BUF_MIXED, PACE_IO_BF16, PACE_IO_F32, PACE_MAX_DP,
-                   PACE_MAX_HEADS, PACE_STATE_BF16, PACE_STATE_FP32, PACE_STATE_QUANT, PaceError, check, lib,
+                   PACE_MAX_HEADS, PACE_STATE_BF16, PACE_STATE_BF16_BUF, PACE_STATE_FP32, PACE_STATE_QUANT, PaceError, check, lib,
                    pace_config, pace_layout)
 
 __all__ = [
@@ -19,7 +19,7 @@ __all__ = [
     "pace_state_get_layout", "pace_prefill_chunk", "pace_decode_step", "pace_flush", "pace_assign_heads",
     "pace_quantize_state", "pace_dequantize_state", "pace_calib_error_energy", "pace_state_export",
     "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_last_error", "pace_version", "PaceState", "PaceError",
-    "PACE_STATE_QUANT", "PACE_STATE_FP32", "PACE_STATE_BF16", "PACE_BUF_INT8", "PACE_BUF_MIXED",
+    "PACE_STATE_QUANT", "PACE_STATE_FP32", "PACE_STATE_BF16", "PACE_STATE_BF16_BUF", "PACE_BUF_INT8", "PACE_BUF_MIXED",
     "PACE_BUF_FP32", "PACE_IO_BF16", "PACE_IO_F32", "PACE_MAX_HEADS", "PACE_MAX_DP",
 ]
 

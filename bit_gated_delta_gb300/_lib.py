@@ -11,7 +11,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libpace.so")
 
 PACE_OK, PACE_ERR_INVALID_ARG, PACE_ERR_UNSUPPORTED, PACE_ERR_STATE, PACE_ERR_CUDA, PACE_ERR_TIMEOUT = range(6)
-PACE_STATE_QUANT, PACE_STATE_FP32, PACE_STATE_BF16 = 0, 1, 2
+PACE_STATE_QUANT, PACE_STATE_FP32, PACE_STATE_BF16, PACE_STATE_BF16_BUF = 0, 1, 2, 3
 PACE_BUF_INT8, PACE_BUF_MIXED, PACE_BUF_FP32 = 0, 1, 2
 PACE_IO_BF16, PACE_IO_F32 = 0, 1
 PACE_MAX_HEADS = 256

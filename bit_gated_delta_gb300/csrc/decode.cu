@@ -1,7 +1,11 @@
-// Decode step and flush of the unquantized test mode (fp32 state, fp32 decode buffer): the same periodic
-// schedule as PACE ([P1] 어떻게 동작하나) with the rounding left out, used to check the replay arithmetic
-// to 1e-4 against the exact recurrence. One CTA per unit, one thread per column j; the fp32 state is
-// streamed from global memory. The buffered tokens are replayed in the reduced per-column form
+// Decode step and flush of the two states kept in plain floating point, on PACE's periodic schedule
+// ([P1] 어떻게 동작하나):
+//   - the unquantized test mode (fp32 state, fp32 decode buffer): the rounding left out, to check the replay
+//     arithmetic to 1e-4 against the exact recurrence;
+//   - the buffered bf16 state ([P1] 전제와 한계: most of the TPOT gain of periodic rounding comes from the decode
+//     buffer with a bf16 state): bf16 state rounded once every dP tokens, int8 decode buffer as in PACE-4.
+// One CTA per unit, one thread per column j; the state is streamed from global memory. The buffered tokens
+// are replayed in the reduced per-column form
 //   u_t = beta_t (v_t - G_t (S^T k_t) - sum_{s<t} (G_t/G_s)(k_s.k_t) u_s),  G_t = a_1 .. a_t,
 //   o   = G_m (S^T q) + sum_s (G_m/G_s)(k_s.q) u_s,
 // and a flush writes S_new = G_m S + sum_s (G_m/G_s) k_s u_s^T.
@@ -13,8 +17,11 @@ namespace pace {
 
 constexpr int VCHUNK = 8;   // dot-product vectors handled per pass over the codes
 
+// Vectors of the dot products (the buffered keys and q), padded to a multiple of 4.
+__host__ __device__ inline int dec_nvp(int dP) { return 4 * ((dP + 1 + 3) / 4); }
+
 struct DecodeSmem {
-  size_t kq, keyf, vf, P, U, kf, csum, vscale, a, beta, gam, Dm, W, cq, ck, red, qf, total;
+  size_t kq, keyf, vf, P, U, kf, csum, vscale, a, beta, gam, Dm, W, cq, ck, red, qf, keyT, Ss, total;
 };
 
 __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
@@ -37,6 +44,8 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
   L.ck = carve(off, (size_t)dP * 4);
   L.red = carve(off, 32 * 4);
   L.qf = carve(off, (size_t)D * 4);
+  L.keyT = carve(off, fp32mode ? 0 : (size_t)D * dec_nvp(dP) * 4);   // bf16 state: [i][vector] fp32 keys, q
+  L.Ss = carve(off, fp32mode ? 0 : (size_t)D * D * 2);                // bf16 state: the unit's state, staged
   L.total = carve(off, 0);
   return L;
 }
@@ -45,7 +54,8 @@ struct DecodeShared {
   int8_t *kq;
   float *keyf, *vf, *P, *U, *kf;
   int *csum;
-  float *vscale, *a, *beta, *gam, *Dm, *W, *cq, *ck, *red, *qf;
+  float *vscale, *a, *beta, *gam, *Dm, *W, *cq, *ck, *red, *qf, *keyT;
+  __nv_bfloat16 *Ss;
 };
 
 __device__ inline DecodeShared decode_shared(unsigned char *base, const DecodeSmem &L) {
@@ -67,6 +77,8 @@ __device__ inline DecodeShared decode_shared(unsigned char *base, const DecodeSm
   s.ck = reinterpret_cast<float *>(base + L.ck);
   s.red = reinterpret_cast<float *>(base + L.red);
   s.qf = reinterpret_cast<float *>(base + L.qf);
+  s.keyT = reinterpret_cast<float *>(base + L.keyT);
+  s.Ss = reinterpret_cast<__nv_bfloat16 *>(base + L.Ss);
   return s;
 }
 
@@ -119,6 +131,51 @@ __device__ void append_token(const PaceDev &st, const PaceIO &io, long unit, int
     bs[3] = sv;
   }
   sh.keyf[(m0 + 1) * D + j] = qx;            // q follows the keys
+}
+
+// Buffered bf16 state: stage buffered tokens 0..m0-1 (int8 key codes, dequantized values, scales).
+template <int D>
+__device__ void load_buffer_i8(const PaceDev &st, long unit, int m0, const DecodeShared &sh) {
+  const int j = threadIdx.x;
+  const int dP = st.dP;
+  const float *bs = st.buf_s + unit * dP * 4;
+  if (j < m0) {
+    sh.a[j] = bs[j * 4 + 0];
+    sh.beta[j] = bs[j * 4 + 1];
+    sh.vscale[j] = bs[j * 4 + 2];
+  }
+  const int8_t *bk = static_cast<const int8_t *>(st.buf_k) + unit * dP * D;
+  const int8_t *bv = static_cast<const int8_t *>(st.buf_v) + unit * dP * D;
+  for (int t = 0; t < m0; ++t) {
+    sh.kq[t * D + j] = bk[t * D + j];
+    sh.vf[t * D + j] = bs[t * 4 + 3] * (float)bv[t * D + j];
+  }
+}
+
+// Buffered bf16 state: quantize the new token into slot m0 ([P1] 어떻게 동작하나: int8 keys and values, one
+// fp32 scale each), in shared and global memory, and stage q.
+template <int D>
+__device__ void append_token_i8(const PaceDev &st, const PaceIO &io, long unit, int m0, const DecodeShared &sh) {
+  const int j = threadIdx.x;
+  const int dP = st.dP;
+  const float kx = load_io(io.k, unit * D + j, st.io);
+  const float vx = load_io(io.v, unit * D + j, st.io);
+  sh.qf[j] = load_io(io.q, unit * D + j, st.io);
+  const float Ak = block_max(fabsf(kx), sh.red);
+  const float Av = block_max(fabsf(vx), sh.red + 32 - D / 32);
+  const int kc = buffer_code(kx, Ak, 127), vc = buffer_code(vx, Av, 127);
+  const float sk = buffer_scale(Ak, 127), sv = buffer_scale(Av, 127);
+  sh.kq[m0 * D + j] = (int8_t)kc;
+  sh.vf[m0 * D + j] = sv * (float)vc;
+  static_cast<int8_t *>(st.buf_k)[(unit * dP + m0) * D + j] = (int8_t)kc;
+  static_cast<int8_t *>(st.buf_v)[(unit * dP + m0) * D + j] = (int8_t)vc;
+  if (j == 0) {
+    const float ax = io.a[unit], bx = io.beta[unit];
+    sh.a[m0] = ax;
+    sh.beta[m0] = bx;
+    sh.vscale[m0] = sk;
+    *reinterpret_cast<float4 *>(st.buf_s + (unit * dP + m0) * 4) = make_float4(ax, bx, sk, sv);
+  }
 }
 
 // Decay products, Gram coefficients, readout and flush coefficients shared by all columns.
@@ -243,6 +300,104 @@ __device__ void fp32_column(const PaceDev &st, const PaceIO &io, long unit, int 
   }
 }
 
+// Buffered bf16 state: the dot products with the unit's bf16 state, staged in shared memory at kernel entry
+// (each element feeds the key codes and q from the transposed table, four vectors per shared-memory load), the
+// replay, and at a rounding S_new = G_m S + sum_s (G_m/G_s) k_s u_s^T written back to global memory as bf16.
+template <int D>
+__device__ void bf16_column(const PaceDev &st, const PaceIO &io, long unit, int mt, int has_token, int do_flush,
+                            const DecodeShared &sh) {
+  const int j = threadIdx.x;
+  const int nvp = dec_nvp(st.dP);
+  __nv_bfloat16 *Sp = static_cast<__nv_bfloat16 *>(st.S) + unit * D * D;
+  const __nv_bfloat16 *Ss = sh.Ss;
+  const int nv = mt + has_token;
+  for (int c0 = 0; c0 < nv; c0 += VCHUNK) {
+    float pf[VCHUNK];
+#pragma unroll
+    for (int t = 0; t < VCHUNK; ++t) pf[t] = 0.0f;
+    if (nv - c0 <= 4) {                           // four vectors or fewer left: one table load per key
+#pragma unroll 8
+      for (int i = 0; i < D; ++i) {
+        const float s = __bfloat162float(Ss[i * D + j]);
+        const float4 k0 = *reinterpret_cast<const float4 *>(sh.keyT + i * nvp + c0);
+        pf[0] = fmaf(s, k0.x, pf[0]);
+        pf[1] = fmaf(s, k0.y, pf[1]);
+        pf[2] = fmaf(s, k0.z, pf[2]);
+        pf[3] = fmaf(s, k0.w, pf[3]);
+      }
+    } else {
+#pragma unroll 4
+      for (int i = 0; i < D; ++i) {
+        const float s = __bfloat162float(Ss[i * D + j]);
+        const float4 k0 = *reinterpret_cast<const float4 *>(sh.keyT + i * nvp + c0);
+        const float4 k1 = *reinterpret_cast<const float4 *>(sh.keyT + i * nvp + c0 + 4);
+        pf[0] = fmaf(s, k0.x, pf[0]);
+        pf[1] = fmaf(s, k0.y, pf[1]);
+        pf[2] = fmaf(s, k0.z, pf[2]);
+        pf[3] = fmaf(s, k0.w, pf[3]);
+        pf[4] = fmaf(s, k1.x, pf[4]);
+        pf[5] = fmaf(s, k1.y, pf[5]);
+        pf[6] = fmaf(s, k1.z, pf[6]);
+        pf[7] = fmaf(s, k1.w, pf[7]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < VCHUNK; ++t) {
+      const int v = c0 + t;
+      if (v < mt) sh.P[v * D + j] = sh.vscale[v] * pf[t];    // key codes times the key scale
+      else if (v < nv) sh.P[v * D + j] = pf[t];               // q
+    }
+  }
+  recurrence<D>(st, io, unit, nv, mt, has_token, 1, sh);
+  if (!do_flush) return;
+  flush_coeffs<D>(mt, 0, sh);
+  __syncthreads();
+  const float gm = sh.gam[mt - 1];
+  for (int i = 0; i < D; ++i) {
+    float x = gm * __bfloat162float(Ss[i * D + j]);
+    for (int s = 0; s < mt; ++s) x = fmaf(sh.kf[s * D + i], sh.U[s * D + j], x);
+    Sp[i * D + j] = __float2bfloat16_rn(x);
+  }
+}
+
+// Buffered bf16 state: one decode step (or a flush) of one unit.
+template <int D>
+__global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const long unit = blockIdx.x;
+  const DecodeSmem L = decode_smem(D, st.dP, 0);
+  const DecodeShared sh = decode_shared(smem, L);
+  const int j = threadIdx.x;
+  {                                               // the unit's bf16 state, all copies in flight at once
+    const char *src = reinterpret_cast<const char *>(static_cast<const __nv_bfloat16 *>(st.S) + unit * D * D);
+    char *dst = reinterpret_cast<char *>(sh.Ss);
+    for (int c = j; c < D * D * 2 / 16; c += D)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + 16 * c)),
+                   "l"(src + 16 * c) : "memory");
+  }
+  const int m0 = st.m[unit];
+  if (m0 < 0 || m0 >= st.dP || (!has_token && m0 == 0)) {
+    asm volatile("cp.async.wait_all;" ::: "memory");   // nothing may land in shared memory after the CTA leaves
+    if (has_token && m0 != 0) store_io(io.o, unit * D + j, 0.0f, st.io);   // corrupted counter: emit zeros
+    return;                                       // (or a flush with nothing pending)
+  }
+  const int mt = m0 + has_token;
+  const int do_flush = !has_token || mt == st.dP;
+  load_buffer_i8<D>(st, unit, m0, sh);
+  if (has_token) append_token_i8<D>(st, io, unit, m0, sh);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  {                                               // keyT[i][v]: key codes of the mt tokens, then q, zero padded
+    const int nvp = dec_nvp(st.dP);
+    for (int v = 0; v < nvp; ++v)
+      sh.keyT[j * nvp + v] = v < mt ? (float)sh.kq[v * D + j] : (v == mt && has_token ? sh.qf[j] : 0.0f);
+  }
+  unit_tables<D>(mt, has_token, 0, st.dP, sh);
+  __syncthreads();
+  bf16_column<D>(st, io, unit, mt, has_token, do_flush, sh);
+  if (j == 0) st.m[unit] = do_flush ? 0 : mt;
+}
+
 template <int D>
 __global__ void __launch_bounds__(D) decode_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -286,9 +441,28 @@ static cudaError_t launch_decode_t(const PaceDev &d, const PaceIO &io, int has_t
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_bf16buf_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  const size_t smem = decode_smem(D, d.dP, 0).total;
+  auto kern = decode_bf16buf_kernel<D>;
+  static size_t opted = 48 * 1024;
+  if (smem > opted) {
+    const size_t most = decode_smem(D, PACE_MAX_DP, 0).total;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    if (e != cudaSuccess) return e;
+    opted = most;
+  }
+  const unsigned units = (unsigned)(d.B * d.H);
+  if (units == 0) return cudaSuccess;
+  kern<<<units, D, smem, s>>>(d, io, has_token);
+  return cudaGetLastError();
+}
+
 }  // namespace pace
 
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
   using namespace pace;
+  if (d.state_mode == PACE_STATE_BF16_BUF)
+    return d.D == 128 ? launch_bf16buf_t<128>(d, io, has_token, s) : launch_bf16buf_t<64>(d, io, has_token, s);
   return d.D == 128 ? launch_decode_t<128>(d, io, has_token, s) : launch_decode_t<64>(d, io, has_token, s);
 }

@@ -62,6 +62,9 @@ pace_status validate_config(const pace_config *c, const uint8_t *mask) {
       break;
     case PACE_STATE_BF16:
       break;
+    case PACE_STATE_BF16_BUF:
+      if (c->buf_mode != PACE_BUF_INT8) return fail(PACE_ERR_UNSUPPORTED, "buffered bf16 state needs the int8 buffer");
+      break;
     default:
       return fail(PACE_ERR_INVALID_ARG, "bad state_mode %d", c->state_mode);
   }
@@ -110,6 +113,11 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
     take(L.S, B * H * D * D * 4);
     take(L.buf_k, B * H * P * D * 4);
     take(L.buf_v, B * H * P * D * 4);
+    take(L.buf_s, B * H * P * 16);
+  } else if (c->state_mode == PACE_STATE_BF16_BUF) {
+    take(L.S, B * H * D * D * 2);
+    take(L.buf_k, B * H * P * D);
+    take(L.buf_v, B * H * P * D);
     take(L.buf_s, B * H * P * 16);
   } else {
     take(L.S, B * H * D * D * 2);
@@ -385,6 +393,7 @@ double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, i
   }
   if (cfg->state_mode == PACE_STATE_FP32) return 32.0 + 0.0;
   if (cfg->state_mode == PACE_STATE_BF16) return 16.0;
+  if (cfg->state_mode == PACE_STATE_BF16_BUF) return 16.0 + (8.0 * D + 8.0 * D + 32.0) / (D * D) * cfg->dP;
   int n8 = 0;
   for (int h = 0; h < cfg->n_heads; ++h) n8 += (head_is_int8 && head_is_int8[h]) ? 1 : 0;
   const double f8 = n8 / H;

@@ -45,7 +45,10 @@ typedef enum {
 enum {
   PACE_STATE_QUANT = 0,      /* PACE: int4/int8 codes + bf16 key-axis group scales (+ zero points) */
   PACE_STATE_FP32 = 1,       /* unquantized test mode: fp32 state, fp32 buffer, same periodic schedule */
-  PACE_STATE_BF16 = 2        /* comparison kernel: bf16 state read and written every token, no buffer */
+  PACE_STATE_BF16 = 2,       /* comparison kernel: bf16 state read and written every token, no buffer */
+  PACE_STATE_BF16_BUF = 3    /* bf16 state rounded once every dP tokens, with the int8 decode buffer: the
+                                decode buffer without the 4-bit state ([P1] 전제와 한계: the pages attribute
+                                most of the TPOT gain to the buffer with a bf16 state) */
 };
 /* Decode-buffer format ([P1] 어떻게 동작하나: int8 keys and values in the uniform configuration, 4-bit keys
  * and bf16 values in the mixed configuration). */
@@ -63,7 +66,7 @@ typedef struct {
   int dP;             /* decode period, 1..PACE_MAX_DP (pages' default 8) */
   int group;          /* key-axis group size g: 32 or 64, divides d_k (PACE-4: 64, PACE-4/8: 32) */
   int zero_point;     /* 0: symmetric codes (PACE-4); 1: integer zero point (PACE-4/8) */
-  int buf_mode;       /* PACE_BUF_*; PACE_STATE_FP32 requires PACE_BUF_FP32 */
+  int buf_mode;       /* PACE_BUF_*; PACE_STATE_FP32 requires PACE_BUF_FP32, PACE_STATE_BF16_BUF PACE_BUF_INT8 */
   int state_mode;     /* PACE_STATE_* */
   int prefill_chunk;  /* tokens rounded together in prefill; must be 256 ([P1] 어떻게 동작하나) */
   int io_dtype;       /* PACE_IO_* for q, k, v, o */
@@ -91,7 +94,7 @@ typedef struct pace_state pace_state;   /* opaque host handle */
  *   buf_s   float  [B][H][dP][4]        a_t, beta_t, key scale, value scale
  *   m       int32  [B][H]               tokens in the buffer
  *   status  int32  [1]                  bit 0: a bounded device wait gave up (see pace_get_status)
- *   S       float/bf16 [B][H][d_k][d_v] state of PACE_STATE_FP32 / PACE_STATE_BF16
+ *   S       float/bf16 [B][H][d_k][d_v] state of PACE_STATE_FP32 / PACE_STATE_BF16 and PACE_STATE_BF16_BUF
  * head_slot[h] is the index of head h inside its pool (codes4 or codes8). */
 typedef struct {
   size_t codes4, codes8, scale, zp, buf_k, buf_v, buf_s, m, S, status;

@@ -99,6 +99,8 @@ def read_blob(state) -> Blob:
 def oracle_cfg(wl: synth.Workload, bits: int = 4, state_mode: int = O.STATE_QUANT) -> O.Cfg:
     if state_mode == O.STATE_QUANT:
         buf = O.BUF_MIXED if wl.mixed_buffer else O.BUF_INT8
+    elif state_mode == O.STATE_BF16_BUF:
+        buf = O.BUF_INT8                             # the library keeps this mode's buffer in int8
     else:
         buf = O.BUF_FP32
     return O.Cfg(d_k=wl.d_k, d_v=wl.d_v, g=wl.g, bits=bits, zero_point=wl.zero_point, dP=wl.dP, buf_mode=buf,
@@ -163,7 +165,7 @@ class PairRun:
                                  io_dtype=P.PACE_IO_BF16 if self.io_bf16 else P.PACE_IO_F32)
         self.state = P.PaceState(self.cfg, wl.B, self.mask if state_mode == 0 else None)
         self.sample = sample if sample is not None else [(b, h) for b in range(wl.B) for h in range(wl.H)]
-        om = {0: O.STATE_QUANT, 1: O.STATE_FP32, 2: O.STATE_BF16}[state_mode]
+        om = {0: O.STATE_QUANT, 1: O.STATE_FP32, 2: O.STATE_BF16, 3: O.STATE_BF16_BUF}[state_mode]
         self.units = {}
         for (b, h) in self.sample:
             c = oracle_cfg(wl, bits=8 if self.mask[h] else 4, state_mode=om)
@@ -245,6 +247,18 @@ class PairRun:
             g.append(gc)
             r.append(rc)
         return code_agreement(np.stack(g), np.stack(r))
+
+    def gpu_state(self) -> np.ndarray:
+        """The resident state of every unit as fp32 [B, H, d_k, d_v] (fp32 and bf16 modes)."""
+        out = self.torch.empty(self.wl.B, self.wl.H, self.wl.d_k, self.wl.d_v, device="cuda")
+        self.P.pace_dequantize_state(self.state.handle, out)
+        return out.cpu().numpy()
+
+    def sync_state_from_gpu(self):
+        """Teacher forcing for the fp32 / bf16 modes: the oracle continues from the GPU's resident state."""
+        S = self.gpu_state().astype(np.float64)
+        for (b, h), u in self.units.items():
+            u.S[...] = S[b, h]
 
     def state_vs_oracle(self) -> float:
         """Relative L2 distance of the resident states (fp32 / bf16 modes)."""
