@@ -150,7 +150,8 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode_mma.cuh", "bit_gated_delta_gb300/csrc/decode_mma_s8.cu", "bit_gated_delta_gb300/csrc/pace_common.cuh",
+DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode_mma.cuh", "bit_gated_delta_gb300/csrc/decode_mma_s8.cu",
+                  "bit_gated_delta_gb300/csrc/decode_col.cu", "bit_gated_delta_gb300/csrc/pace_common.cuh",
                   "bit_gated_delta_gb300/csrc/pace_internal.h"]
 
 

@@ -1319,11 +1319,11 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
 }
 
 template <int D, int G, int ZP, int MX>
-static cudaError_t launch_mma_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+static cudaError_t launch_mma_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, bool int4_pool = true) {
   const MmaSmem L = mma_smem(D, G, d.dP, MX, ZP);
   const size_t smem = (size_t)DM_WARPS * L.total;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = launch_pool<D, G, 4, ZP, MX>(d, io, has_token, s, smem);
+  cudaError_t e = int4_pool ? launch_pool<D, G, 4, ZP, MX>(d, io, has_token, s, smem) : cudaSuccess;
   if (e == cudaSuccess) e = launch_pool<D, G, 8, ZP, MX>(d, io, has_token, s, smem);
   return e;
 }
@@ -1331,14 +1331,15 @@ static cudaError_t launch_mma_t(const PaceDev &d, const PaceIO &io, int has_toke
 // Every (D, G) of one zero-point mode and buffer format; each combination is instantiated in a translation
 // unit of its own so that they compile in parallel.
 template <int ZP, int MX>
-cudaError_t launch_quant_zm(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+cudaError_t launch_quant_zm(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, bool int4_pool = true) {
   if (d.D == 128)
-    return d.G == 64 ? launch_mma_t<128, 64, ZP, MX>(d, io, has_token, s) : launch_mma_t<128, 32, ZP, MX>(d, io, has_token, s);
+    return d.G == 64 ? launch_mma_t<128, 64, ZP, MX>(d, io, has_token, s, int4_pool)
+                     : launch_mma_t<128, 32, ZP, MX>(d, io, has_token, s, int4_pool);
   return d.G == 64 ? launch_mma_t<64, 64, ZP, MX>(d, io, has_token, s) : launch_mma_t<64, 32, ZP, MX>(d, io, has_token, s);
 }
-extern template cudaError_t launch_quant_zm<0, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
-extern template cudaError_t launch_quant_zm<0, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);
-extern template cudaError_t launch_quant_zm<1, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
-extern template cudaError_t launch_quant_zm<1, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_quant_zm<0, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t, bool);
+extern template cudaError_t launch_quant_zm<0, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t, bool);
+extern template cudaError_t launch_quant_zm<1, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t, bool);
+extern template cudaError_t launch_quant_zm<1, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t, bool);
 
 }  // namespace pace

@@ -2,5 +2,5 @@
 #include "decode_mma.cuh"
 
 namespace pace {
-template cudaError_t launch_quant_zm<1, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+template cudaError_t launch_quant_zm<1, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t, bool);
 }  // namespace pace

@@ -47,6 +47,10 @@ struct PaceIO {
 // Kernel launchers (each returns the launch status; nothing synchronises).
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
+// Quantized decode of the int4 heads of a d = 128 state with an int8 buffer and dP <= 8 on tcgen05, one thread
+// per state column (pace_decode_col_supported says whether a state qualifies).
+bool pace_decode_col_supported(const PaceDev &d);
+cudaError_t pace_launch_decode_col(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 // Tensor-core chunk prefill (d_k = d_v = 128, bf16 I/O); pace_prefill_tc_supported says whether it applies.
