@@ -55,6 +55,13 @@ __host__ __device__ constexpr uint32_t core_off(int r, int k, int kdim) {
   return (uint32_t)((r >> 3) * (kdim >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros (padding tokens).
+__device__ __forceinline__ void cp16_zfill(void *dst_smem, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&v);
@@ -191,30 +198,34 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
   }
   tmem_wait_st();
 
+  // the k, q rows (K-major cores) and v rows of the sub-chunk starting at token s0, as asynchronous copies;
+  // padding tokens (s0 + t >= n) are zeros
+  auto issue_rows = [&](int s0) {
+    const int ns = min(T, n - s0);
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {                    // 64 rows x 16 chunks of 16 bytes
+      const int c = tid + NT * it, row = c >> 4, c8 = c & 15, t = row & (T - 1);
+      const bool in = t < ns;
+      const __nv_bfloat16 *src = (row < T ? gk : gq) + ((unit * n + s0 + (in ? t : 0)) * D + 8 * c8);
+      cp16_zfill(smem + OFF_X + core_off(row, 8 * c8, D), src, in ? 16u : 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {                    // 32 rows x 16 chunks
+      const int c = tid + NT * it, t = c >> 4, c8 = c & 15;
+      const bool in = t < ns;
+      cp16_zfill(smem + OFF_V + (t * D + 8 * c8) * 2, gv + ((unit * n + s0 + (in ? t : 0)) * D + 8 * c8), in ? 16u : 0u);
+    }
+  };
+  if (n > 0) issue_rows(0);
+
   bool ok = true;
   uint32_t pending = 0;                                 // parity of an MMA group whose wait gave up
 #pragma unroll 1
   for (int t0 = 0; t0 < n && ok; t0 += T) {
     const int nt = min(T, n - t0);
-    // ---- (a) the sub-chunk's k and q rows (K-major cores), v rows, a and beta; padding tokens are a = 1,
-    // beta = 0, k = q = v = 0, which leave the state unchanged.
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {                    // 64 rows x 16 chunks of 16 bytes
-      const int c = tid + NT * it, row = c >> 4, c8 = c & 15, t = row & (T - 1);
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (t < nt) {
-        const __nv_bfloat16 *src = (row < T ? gk : gq) + ((unit * n + t0 + t) * D + 8 * c8);
-        val = *reinterpret_cast<const uint4 *>(src);
-      }
-      *reinterpret_cast<uint4 *>(smem + OFF_X + core_off(row, 8 * c8, D)) = val;
-    }
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {                    // 32 rows x 16 chunks
-      const int c = tid + NT * it, t = c >> 4, c8 = c & 15;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (t < nt) val = *reinterpret_cast<const uint4 *>(gv + ((unit * n + t0 + t) * D + 8 * c8));
-      *reinterpret_cast<uint4 *>(smem + OFF_V + (t * D + 8 * c8) * 2) = val;
-    }
+    // ---- (a) the sub-chunk's rows (in flight since the previous sub-chunk's update), a and beta; padding tokens
+    // are a = 1, beta = 0, k = q = v = 0, which leave the state unchanged.
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (warp == 0) {
       const float a = lane < nt ? io.a[unit * n + t0 + lane] : 1.0f;
       const float be = lane < nt ? io.beta[unit * n + t0 + lane] : 0.0f;
@@ -377,6 +388,7 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     fence_smem_to_async();
     fence_before_sync();
     __syncthreads();
+    if (t0 + T < n) issue_rows(t0 + T);                 // the rows and keys of this sub-chunk are done with
 
     // ---- (j) S^T += (R u)^T k : M = columns, N = keys, K = tokens
     if (tid == 0) {
@@ -425,6 +437,7 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     atomicOr(st.status, 1);
     mbar_wait(bar, pending, WAIT_NS);                   // let the MMAs in flight drain before TMEM is released
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");      // no copy may land after the CTA leaves
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
