@@ -310,9 +310,10 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
         const float d = __uint_as_float(s < 16 ? d0[s] : d1[s - 16]);
         out[s] = (s < t || (isq && s == t)) ? Rr * d : 0.0f;
       }
-      float *row = reinterpret_cast<float *>(smem + (isq ? OFF_WQ : OFF_WK)) + t * T;
+      // stored transposed, [s][t]: the recurrence sweeps by s and reads row s four tokens per load
+      float *tab = reinterpret_cast<float *>(smem + (isq ? OFF_WQ : OFF_WK));
 #pragma unroll
-      for (int s = 0; s < T; s += 4) *reinterpret_cast<float4 *>(row + s) = make_float4(out[s], out[s + 1], out[s + 2], out[s + 3]);
+      for (int s = 0; s < T; ++s) tab[s * T + t] = out[s];
     }
     float w[T], p[T];
     {
@@ -330,34 +331,44 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     }
     __syncthreads();
 
-    // ---- (h) the per-column recurrence and the outputs
+    // ---- (h) the per-column recurrence and the outputs, swept by s (right-looking): once u_s is known it is
+    // subtracted from every later token's residual R_t and added to every output O_t with t >= s, so the
+    // dependent chain per token is one multiply-add and one multiply; the other updates are independent.
     float u[T];
-    const float *wk = reinterpret_cast<const float *>(smem + OFF_WK);
-    const float *wq = reinterpret_cast<const float *>(smem + OFF_WQ);
-    const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_V);
+    {
+      const float *wkT = reinterpret_cast<const float *>(smem + OFF_WK);    // [s][t] = R_ts K_ts (t > s)
+      const float *wqT = reinterpret_cast<const float *>(smem + OFF_WQ);    // [s][t] = R_ts Q_ts (t >= s)
+      const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(smem + OFF_V);
+      float *R = w, *O = p;                             // in place: R_t = v_t - G_t w_t, O_t = G_t p_t
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const float gt = sc[2 * T + t];
-      float acc = fmaf(-gt, w[t], __bfloat162float(vs[t * D + j]));
-#pragma unroll
-      for (int s = 0; s < t; s += 4) {
-        const float4 c4 = *reinterpret_cast<const float4 *>(wk + t * T + s);
-        acc = fmaf(-c4.x, u[s], acc);
-        if (s + 1 < t) acc = fmaf(-c4.y, u[s + 1], acc);
-        if (s + 2 < t) acc = fmaf(-c4.z, u[s + 2], acc);
-        if (s + 3 < t) acc = fmaf(-c4.w, u[s + 3], acc);
+      for (int t = 0; t < T; ++t) {
+        const float gt = sc[2 * T + t];
+        R[t] = fmaf(-gt, w[t], __bfloat162float(vs[t * D + j]));
+        O[t] = gt * p[t];
       }
-      u[t] = sc[T + t] * acc;
-      float o = gt * p[t];
 #pragma unroll
-      for (int s = 0; s <= t; s += 4) {
-        const float4 c4 = *reinterpret_cast<const float4 *>(wq + t * T + s);
-        o = fmaf(c4.x, u[s], o);
-        if (s + 1 <= t) o = fmaf(c4.y, u[s + 1], o);
-        if (s + 2 <= t) o = fmaf(c4.z, u[s + 2], o);
-        if (s + 3 <= t) o = fmaf(c4.w, u[s + 3], o);
+      for (int s = 0; s < T; ++s) {
+        u[s] = sc[T + s] * R[s];
+#pragma unroll
+        for (int t4 = (s + 1) & ~3; t4 < T; t4 += 4) {
+          const float4 c = *reinterpret_cast<const float4 *>(wkT + s * T + t4);
+          if (t4 + 0 > s) R[t4 + 0] = fmaf(-c.x, u[s], R[t4 + 0]);
+          if (t4 + 1 > s) R[t4 + 1] = fmaf(-c.y, u[s], R[t4 + 1]);
+          if (t4 + 2 > s) R[t4 + 2] = fmaf(-c.z, u[s], R[t4 + 2]);
+          if (t4 + 3 > s) R[t4 + 3] = fmaf(-c.w, u[s], R[t4 + 3]);
+        }
+#pragma unroll
+        for (int t4 = s & ~3; t4 < T; t4 += 4) {
+          const float4 c = *reinterpret_cast<const float4 *>(wqT + s * T + t4);
+          if (t4 + 0 >= s) O[t4 + 0] = fmaf(c.x, u[s], O[t4 + 0]);
+          if (t4 + 1 >= s) O[t4 + 1] = fmaf(c.y, u[s], O[t4 + 1]);
+          if (t4 + 2 >= s) O[t4 + 2] = fmaf(c.z, u[s], O[t4 + 2]);
+          if (t4 + 3 >= s) O[t4 + 3] = fmaf(c.w, u[s], O[t4 + 3]);
+        }
       }
-      if (t < nt) go[(unit * n + t0 + t) * D + j] = __float2bfloat16_rn(o);
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+        if (t < nt) go[(unit * n + t0 + t) * D + j] = __float2bfloat16_rn(O[t]);
     }
 
     // ---- (i) update operands: (R_Tt u_t)^T parts (row j, K = tokens) and k^T (row i = tid, K = tokens)
