@@ -61,6 +61,7 @@ def lib():
         L.orc_bf16_rn.restype = C.c_float
         L.orc_bf16_rn.argtypes = [C.c_float]
         L.orc_error_energy.restype = C.c_double
+        L.orc_error_energy_axis.restype = C.c_double
         L.orc_retained_error.restype = C.c_double
         L.orc_retained_error.argtypes = [C.c_double, C.c_double, C.c_int]
         L.orc_payload_bits.restype = C.c_double
@@ -262,6 +263,13 @@ def error_energy(cfg: Cfg, S32) -> float:
     S32 = _f32(S32)
     c = cfg.c()
     return float(lib().orc_error_energy(C.byref(c), _p(S32, C.c_float)))
+
+
+def error_energy_axis(cfg: Cfg, S32, axis: int) -> float:
+    """||Q(S) - S||_F^2 with the groups along the key axis (axis 0, PACE) or the value axis (axis 1, baseline)."""
+    S32 = _f32(S32)
+    c = cfg.c()
+    return float(lib().orc_error_energy_axis(C.byref(c), _p(S32, C.c_float), int(axis)))
 
 
 def retained_error(e_h: float, a_h: float, dP: int) -> float:

@@ -355,6 +355,25 @@ double orc_error_energy(const orc_cfg *cfg, const float *S32) {
   return e;
 }
 
+/* The baseline the pages contrast the key-axis groups with ([P1] 무엇과 다른가: the scale is shared   */
+/* by g consecutive elements along the key axis of one column, so an outlier value channel does not */
+/* widen the groups of the other channels): groups of g consecutive elements along the VALUE axis   */
+/* of one key row. Those are exactly the key-axis groups of the transposed state, so the error is   */
+/* orc_error_energy of S^T under the same quantizer (d_k and d_v swapped). axis 0: key axis.         */
+double orc_error_energy_axis(const orc_cfg *cfg, const float *S32, int axis) {
+  if (axis == 0) return orc_error_energy(cfg, S32);
+  const int dk = cfg->d_k, dv = cfg->d_v;
+  float *T = (float *)malloc(sizeof(float) * (long)dk * dv);
+  for (int i = 0; i < dk; ++i)
+    for (int j = 0; j < dv; ++j) T[(long)j * dk + i] = S32[(long)i * dv + j];
+  orc_cfg ct = *cfg;
+  ct.d_k = dv;
+  ct.d_v = dk;
+  const double e = orc_error_energy(&ct, T);
+  free(T);
+  return e;
+}
+
 /* One rounding leaves e_h; it decays by a_h^(2 dP) in energy per period, so the error still held  */
 /* is the geometric sum e_h (1 + a^(2dP) + a^(4dP) + ...) = e_h / (1 - a_h^(2 dP)).                  */
 double orc_retained_error(double e_h, double a_h, int dP) {

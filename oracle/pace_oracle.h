@@ -90,6 +90,8 @@ void orc_prefill(const orc_cfg *cfg, orc_unit *u, int n, const float *q, const f
 
 /* Error energy of one rounding of an fp32 state: sum (deq(Q(S)) - S)^2. */
 double orc_error_energy(const orc_cfg *cfg, const float *S32);
+/* Same with the groups along the value axis of one key row (axis 1), the baseline grouping; axis 0 = key axis. */
+double orc_error_energy_axis(const orc_cfg *cfg, const float *S32, int axis);
 /* Head ranking by E_h = e_h / (1 - a_h^(2 dP)); marks the floor(H*frac) largest (ties: lower index). */
 void orc_assign_heads(const double *e_h, const double *a_h, int H, int dP, double frac, uint8_t *mask);
 /* Retained error E_h of one head (closed form; +inf when a_h >= 1). */

@@ -555,6 +555,39 @@ def _golden():
         return json.load(f)
 
 
+@pytest.mark.parametrize("bits,zp,g", [(4, 0, 8), (4, 1, 8), (8, 0, 4), (4, 0, 16)])
+def test_value_axis_error_is_the_row_segment_quantizer(bits, zp, g):
+    """Value-axis groups: brute force over every key row's g-element segments with the group quantizer."""
+    dk, dv = 16, 32
+    cfg = O.Cfg(d_k=dk, d_v=dv, g=g, bits=bits, zero_point=zp)
+    S = (RNG.standard_normal((dk, dv)) * np.where(np.arange(dv) % 7 == 3, 8.0, 1.0)).astype(np.float32)
+    e = 0.0
+    for i in range(dk):
+        for c0 in range(0, dv, g):
+            x = S[i, c0:c0 + g]
+            if zp:
+                s_, z, c = O.quant_group_zp(x, bits)
+                deq = np.float64(s_) * (c.astype(np.float64) - z)
+            else:
+                s_, c = O.quant_group_sym(x, bits)
+                deq = np.float64(s_) * c.astype(np.float64)
+            e += float(np.sum((deq - x.astype(np.float64)) ** 2))
+    assert O.error_energy_axis(cfg, S, 1) == pytest.approx(e, rel=1e-12, abs=1e-30)
+    assert O.error_energy_axis(cfg, S, 0) == O.error_energy(cfg, S)
+
+
+def test_key_axis_groups_isolate_outlier_columns():
+    """A state whose columns have very different magnitudes (outlier value channels): key-axis groups (one
+    column each) leave the small columns at their own scale, value-axis groups mix them with the outliers."""
+    dk, dv = 64, 64
+    cfg = O.Cfg(d_k=dk, d_v=dv, g=32, bits=4)
+    mag = np.ones(dv)
+    mag[[3, 17, 40, 61]] = 8.0
+    S = (RNG.standard_normal((dk, dv)) * mag[None, :]).astype(np.float32)
+    ek, ev = O.error_energy_axis(cfg, S, 0), O.error_energy_axis(cfg, S, 1)
+    assert ev > 2.0 * ek
+
+
 def test_payload_bits_pace48_is_printed_value():
     gd = _golden()["payload_bits_pace48"]
     s = gd["setup"]
