@@ -439,6 +439,57 @@ def prefill_longctx(P, torch, n_tokens=32768, distinct=8):
             "note": "tensor-core chunk prefill; inputs drawn on the device, 8 distinct chunks reused"}
 
 
+def synthetic_error_study(P, torch, prefill_tokens=32768, decode_tokens=1024):
+    """The pages' two claims on the synthetic column-outlier states (long-context shape: 48 heads, d=128,
+    batch 16, slow decay): (1) the quantization error of the prefilled fp32 state with the scale shared along the
+    key axis (PACE) and along the value axis (baseline), per head; (2) the drift of PACE-4 outputs against the
+    unquantized state over `decode_tokens` decode steps for rounding periods dP = 1 (per-token rounding), 8, 32.
+    All states start from the same prefill inputs (8 distinct device-drawn chunks reused cyclically) and decode
+    the same device-drawn tokens."""
+    import synth
+    wl = synth.workload("longctx")
+    B, H, D = wl.B, wl.H, wl.d_k
+    chunks = [synth.device_chunk_inputs(wl, 256 * c, 256) for c in range(8)]
+    dec = synth.device_chunk_inputs(wl, prefill_tokens, decode_tokens)
+    modes = {"fp32": (P.PACE_STATE_FP32, P.PACE_BUF_FP32, 8)}
+    for dP in (1, 8, 32):
+        modes[f"pace4_dP{dP}"] = (P.PACE_STATE_QUANT, P.PACE_BUF_INT8, dP)
+    states = {}
+    o = torch.empty(B, H, 256, D, dtype=torch.bfloat16, device="cuda")
+    for name, (sm, bm, dP) in modes.items():
+        st = P.PaceState(P.make_config(H, D, B, dP=dP, group=wl.g, state_mode=sm, buf_mode=bm), B)
+        for c in range(prefill_tokens // 256):
+            x = chunks[c % 8]
+            st.prefill_chunk(x["q"], x["k"], x["v"], x["a"], x["beta"], o)
+        states[name] = st
+    ek = torch.zeros(B * H, device="cuda")
+    ev = torch.zeros(B * H, device="cuda")
+    P.pace_calib_error_energy_axis(states["fp32"].handle, 4, wl.g, 0, 0, ek)
+    P.pace_calib_error_energy_axis(states["fp32"].handle, 4, wl.g, 0, 1, ev)
+    ratio = (ev / ek.clamp_min(1e-30)).cpu().numpy()
+    outs = {}
+    tail = {name: [] for name in modes if name != "fp32"}
+    for t in range(decode_tokens):
+        x = {k: v[:, :, t].contiguous() for k, v in dec.items()}
+        for name, st in states.items():
+            ob = torch.empty(B, H, D, dtype=torch.bfloat16, device="cuda")
+            st.decode_step(x["q"], x["k"], x["v"], x["a"], x["beta"], ob)
+            outs[name] = ob.float()
+        if t >= decode_tokens - 256:
+            r = outs["fp32"]
+            rn = float(torch.linalg.vector_norm(r))
+            for name in tail:
+                tail[name].append(float(torch.linalg.vector_norm(outs[name] - r)) / rn)
+    drift = {name: {"rel_l2_last_256_mean": float(np.mean(v)), "rel_l2_final": v[-1]} for name, v in tail.items()}
+    for st in states.values():
+        st.close()
+    return {"B": B, "H": H, "d": D, "prefill_tokens": prefill_tokens, "decode_tokens": decode_tokens,
+            "error_value_over_key_axis": {"mean": float(ratio.mean()), "median": float(np.median(ratio)),
+                                          "min": float(ratio.min()), "heads_key_axis_lower": float(np.mean(ratio > 1))},
+            "drift_vs_unquantized": drift,
+            "note": "fp32 unquantized reference vs PACE-4 (g=64, int8 buffer) at dP 1/8/32; bf16 outputs"}
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -512,6 +563,7 @@ def main():
             torch.cuda.empty_cache()
         extra["sweep_24x16"] = batch_sweep(P, torch)
         extra["prefill_longctx"] = prefill_longctx(P, torch)
+        extra["synthetic_error"] = synthetic_error_study(P, torch)
 
     cb = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:

@@ -17,7 +17,8 @@ from ._lib import (PACE_BUF_FP32, PACE_BUF_INT8, PACE_BUF_MIXED, PACE_IO_BF16, P
 __all__ = [
     "pace_config", "make_config", "pace_state_bytes", "pace_state_alloc", "pace_state_free",
     "pace_state_get_layout", "pace_prefill_chunk", "pace_decode_step", "pace_flush", "pace_assign_heads",
-    "pace_quantize_state", "pace_dequantize_state", "pace_calib_error_energy", "pace_state_export",
+    "pace_quantize_state", "pace_dequantize_state", "pace_calib_error_energy", "pace_calib_error_energy_axis",
+    "pace_state_export",
     "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_last_error", "pace_version", "PaceState", "PaceError",
     "PACE_STATE_QUANT", "PACE_STATE_FP32", "PACE_STATE_BF16", "PACE_STATE_BF16_BUF", "PACE_BUF_INT8", "PACE_BUF_MIXED",
     "PACE_BUF_FP32", "PACE_IO_BF16", "PACE_IO_F32", "PACE_MAX_HEADS", "PACE_MAX_DP",
@@ -120,6 +121,11 @@ def pace_dequantize_state(handle, S_out, stream=None) -> None:
 
 def pace_calib_error_energy(handle, bits: int, group: int, zero_point: int, e_out, stream=None) -> None:
     check(lib().pace_calib_error_energy(handle, bits, group, zero_point, _ptr(e_out), _stream(stream)))
+
+
+def pace_calib_error_energy_axis(handle, bits: int, group: int, zero_point: int, axis: int, e_out,
+                                 stream=None) -> None:
+    check(lib().pace_calib_error_energy_axis(handle, bits, group, zero_point, axis, _ptr(e_out), _stream(stream)))
 
 
 def pace_state_export(handle, dst, nbytes: int, stream=None) -> None:

@@ -58,6 +58,7 @@ _SIGS = {
     "pace_quantize_state": (_I, [_VP, _VP, _VP]),
     "pace_dequantize_state": (_I, [_VP, _VP, _VP]),
     "pace_calib_error_energy": (_I, [_VP, _I, _I, _I, _VP, _VP]),
+    "pace_calib_error_energy_axis": (_I, [_VP, _I, _I, _I, _I, _VP, _VP]),
     "pace_state_export": (_I, [_VP, _VP, _SZ, _VP]),
     "pace_state_import": (_I, [_VP, _VP, _SZ, _VP]),
     "pace_resident_bits": (_D, [C.POINTER(pace_config), _PU8, _I]),

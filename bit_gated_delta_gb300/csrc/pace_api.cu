@@ -310,6 +310,11 @@ pace_status pace_dequantize_state(const pace_state *state, float *S_out, void *s
 
 pace_status pace_calib_error_energy(const pace_state *state, int bits, int group, int zero_point, float *e_out,
                                     void *stream) {
+  return pace_calib_error_energy_axis(state, bits, group, zero_point, 0, e_out, stream);
+}
+
+pace_status pace_calib_error_energy_axis(const pace_state *state, int bits, int group, int zero_point, int axis,
+                                         float *e_out, void *stream) {
   pace_status st = check_state(state);
   if (st != PACE_OK) return st;
   if (state->cfg.state_mode != PACE_STATE_FP32)
@@ -318,8 +323,9 @@ pace_status pace_calib_error_energy(const pace_state *state, int bits, int group
   if ((group != 32 && group != 64) || state->cfg.d_k % group)
     return fail(PACE_ERR_INVALID_ARG, "group %d not supported for d_k %d", group, state->cfg.d_k);
   if (zero_point != 0 && zero_point != 1) return fail(PACE_ERR_INVALID_ARG, "zero_point must be 0 or 1");
+  if (axis != 0 && axis != 1) return fail(PACE_ERR_INVALID_ARG, "axis must be 0 (key axis) or 1 (value axis)");
   if (!e_out) return fail(PACE_ERR_INVALID_ARG, "e_out is NULL");
-  cudaError_t e = pace_launch_calib(state->dev, bits, group, zero_point, e_out, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pace_launch_calib(state->dev, bits, group, zero_point, axis, e_out, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "calibration launch");
   return ok();
 }

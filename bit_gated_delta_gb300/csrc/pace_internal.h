@@ -58,5 +58,5 @@ bool pace_prefill_tc_supported(const PaceDev &d);
 cudaError_t pace_launch_prefill_tc(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s);
 cudaError_t pace_launch_dequantize_state(const PaceDev &d, float *S, cudaStream_t s);
-cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, float *e_out,
+cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, int axis, float *e_out,
                               cudaStream_t s);

@@ -82,8 +82,10 @@ __global__ void __launch_bounds__(D) dequantize_state_kernel(const PaceDev st, f
   }
 }
 
-template <int D, int G, int BITS>
+template <int D, int G, int BITS, int AXIS>
 __global__ void __launch_bounds__(D) calib_kernel(const PaceDev st, int zero_point, float *e_out) {
+  // AXIS 0: thread j quantizes the key-axis groups of column j (PACE); AXIS 1: thread i quantizes the groups of
+  // g consecutive elements along the value axis of key row i (the baseline grouping)
   constexpr int NG = D / G;
   __shared__ float red[32];
   const long unit = blockIdx.x;
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(D) calib_kernel(const PaceDev st, int zero_poi
   for (int g = 0; g < NG; ++g) {
     float x[G];
 #pragma unroll
-    for (int ii = 0; ii < G; ++ii) x[ii] = Sg[(g * G + ii) * D + j];
+    for (int ii = 0; ii < G; ++ii) x[ii] = AXIS == 0 ? Sg[(g * G + ii) * D + j] : Sg[j * D + g * G + ii];
     uint32_t uq[G];
     float s;
     int z;
@@ -115,16 +117,16 @@ __global__ void __launch_bounds__(D) calib_kernel(const PaceDev st, int zero_poi
   }
 }
 
-template <int D>
+template <int D, int AXIS>
 static cudaError_t launch_calib_t(const PaceDev &d, int bits, int group, int zp, float *e, cudaStream_t s) {
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
   if (group == 64) {
-    if (bits == 8) calib_kernel<D, 64, 8><<<units, D, 0, s>>>(d, zp, e);
-    else calib_kernel<D, 64, 4><<<units, D, 0, s>>>(d, zp, e);
+    if (bits == 8) calib_kernel<D, 64, 8, AXIS><<<units, D, 0, s>>>(d, zp, e);
+    else calib_kernel<D, 64, 4, AXIS><<<units, D, 0, s>>>(d, zp, e);
   } else {
-    if (bits == 8) calib_kernel<D, 32, 8><<<units, D, 0, s>>>(d, zp, e);
-    else calib_kernel<D, 32, 4><<<units, D, 0, s>>>(d, zp, e);
+    if (bits == 8) calib_kernel<D, 32, 8, AXIS><<<units, D, 0, s>>>(d, zp, e);
+    else calib_kernel<D, 32, 4, AXIS><<<units, D, 0, s>>>(d, zp, e);
   }
   return cudaGetLastError();
 }
@@ -159,8 +161,11 @@ cudaError_t pace_launch_dequantize_state(const PaceDev &d, float *S, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, float *e_out,
+cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, int axis, float *e_out,
                               cudaStream_t s) {
-  return d.D == 128 ? launch_calib_t<128>(d, bits, group, zero_point, e_out, s)
-                    : launch_calib_t<64>(d, bits, group, zero_point, e_out, s);
+  if (axis == 1)
+    return d.D == 128 ? launch_calib_t<128, 1>(d, bits, group, zero_point, e_out, s)
+                      : launch_calib_t<64, 1>(d, bits, group, zero_point, e_out, s);
+  return d.D == 128 ? launch_calib_t<128, 0>(d, bits, group, zero_point, e_out, s)
+                    : launch_calib_t<64, 0>(d, bits, group, zero_point, e_out, s);
 }

@@ -154,6 +154,13 @@ pace_status pace_dequantize_state(const pace_state *state, float *S_out, void *s
  * PACE_STATE_FP32 handle, with the key-axis quantizer (bits, group, zero_point). e_out: device, fp32. */
 pace_status pace_calib_error_energy(const pace_state *fp32_state, int bits, int group, int zero_point,
                                     float *e_out, void *stream);
+/* The same error energy with the groups along the key axis of one column (axis 0, PACE: the call above) or
+ * along the value axis of one key row (axis 1): the grouping the pages contrast PACE's with ([P1] 무엇과
+ * 다른가: sharing the scale along the key axis keeps an outlier value channel from widening the groups of the
+ * other channels). Same arguments and errors as pace_calib_error_energy; axis outside {0, 1} is
+ * PACE_ERR_INVALID_ARG. */
+pace_status pace_calib_error_energy_axis(const pace_state *fp32_state, int bits, int group, int zero_point, int axis,
+                                         float *e_out, void *stream);
 
 /* Checkpoint / resume: copy the whole resident region (codes, scales, zero points, buffers, m) to or
  * from `bytes` bytes at dst/src, which may be host or device memory. Enqueued on `stream`. */

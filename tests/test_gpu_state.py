@@ -116,6 +116,28 @@ def test_calibration_error_energy(P, bits, g, zp):
     np.testing.assert_allclose(got, ref, rtol=1e-4)
 
 
+@pytest.mark.parametrize("bits,g,zp", [(4, 64, 0), (4, 32, 1), (8, 32, 0)])
+def test_value_axis_error_energy(P, bits, g, zp):
+    """The baseline grouping (g consecutive elements along the value axis of a key row) against the oracle, and
+    on column-outlier states its error is above PACE's key-axis grouping (in total and for most units)."""
+    import torch
+    rng = np.random.default_rng(bits * 1000 + g + zp)
+    B, H, D = 2, 6, 128
+    cfg = P.make_config(H, D, B, group=64, state_mode=P.PACE_STATE_FP32, buf_mode=P.PACE_BUF_FP32)
+    st = P.PaceState(cfg, B)
+    S = column_outlier_states(rng, B, H, D, 0.1)
+    P.pace_quantize_state(st.handle, torch.from_numpy(S).cuda())
+    ev = torch.zeros(B * H, device="cuda")
+    ek = torch.zeros(B * H, device="cuda")
+    P.pace_calib_error_energy_axis(st.handle, bits, g, zp, 1, ev)
+    P.pace_calib_error_energy_axis(st.handle, bits, g, zp, 0, ek)
+    ocfg = O.Cfg(d_k=D, d_v=D, g=g, bits=bits, zero_point=zp)
+    ref = np.array([O.error_energy_axis(ocfg, S[b, h], 1) for b in range(B) for h in range(H)])
+    np.testing.assert_allclose(ev.cpu().numpy(), ref, rtol=1e-4)
+    ev, ek = ev.cpu().numpy(), ek.cpu().numpy()
+    assert ev.sum() > 1.2 * ek.sum() and np.mean(ev > ek) >= 0.75
+
+
 def test_fresh_state_is_zero(P):
     import torch
     for zp in (0, 1):
