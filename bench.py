@@ -490,6 +490,68 @@ def synthetic_error_study(P, torch, prefill_tokens=32768, decode_tokens=1024):
             "note": "fp32 unquantized reference vs PACE-4 (g=64, int8 buffer) at dP 1/8/32; bf16 outputs"}
 
 
+def shared_key_heads(P, torch, peak, B=64, H=32, Hk=16, steps=2000):
+    """PACE-4 decode with shared key heads (gamma = H / Hk value heads per key head, one buffered key copy per key
+    head): the same workload shape as the default line with Hk key heads; rotating state sets as there."""
+    import synth
+    wl = synth.workload("pace4", B=B)
+    cfg = P.make_config(H, 128, B, dP=8, group=64, key_heads=Hk)
+    per = P.pace_state_bytes(cfg)
+    R = max(2, -(-ROTATE_TARGET // per))
+    R = -(-R // 8) * 8
+    states = [P.PaceState(cfg, B) for _ in range(R)]
+    o = torch.empty(B, H, 256, 128, dtype=torch.bfloat16, device="cuda")
+    for c in range(2):
+        x = synth.device_chunk_inputs(wl, 256 * c, 256)
+        states[0].prefill_chunk(x["q"][:, ::H // Hk].contiguous(), x["k"][:, ::H // Hk].contiguous(), x["v"], x["a"],
+                                x["beta"], o)
+    for st in states[1:]:
+        st.region().copy_(states[0].region())
+    xs = synth.device_chunk_inputs(wl, 512, 8)
+    toks = [{k: v[:, :, i].contiguous() for k, v in xs.items()} for i in range(8)]
+    for t in toks:
+        t["q"] = t["q"][:, ::H // Hk].contiguous()
+        t["k"] = t["k"][:, ::H // Hk].contiguous()
+    ob = torch.empty(B, H, 128, dtype=torch.bfloat16, device="cuda")
+    for r, st in enumerate(states):
+        for i in range(r % 8):
+            x = toks[i]
+            st.decode_step(x["q"], x["k"], x["v"], x["a"], x["beta"], ob)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(2):
+            x = toks[i]
+            states[i].decode_step(x["q"], x["k"], x["v"], x["a"], x["beta"], ob)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for i in range(R * 8):
+            x = toks[i % 8]
+            states[i % R].decode_step(x["q"], x["k"], x["v"], x["a"], x["beta"], ob)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, steps // (R * 8))
+    ev0.record()
+    for _ in range(n):
+        g.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / (n * R * 8)
+    for st in states:
+        st.close()
+    # bytes per unit-step: as PACE-4 with the key rows of the buffer read and written once per key head
+    D = 128
+    full = decode_bytes_period_avg(D, 64, 8)
+    key_rows = (sum(m0 for m0 in range(8)) / 8 + 1) * D     # buffered key bytes read + written per unit-step
+    alg = B * H * (full - key_rows * (1 - Hk / H))
+    return {"B": B, "H": H, "key_heads": Hk, "tokens_per_s": B / (ms * 1e-3), "ms_per_step": ms,
+            "achieved_gbs": alg / (ms * 1e-3) / 1e9, "frac": alg / (ms * 1e-3) / 1e9 / peak, "rotating_sets": R}
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -564,6 +626,7 @@ def main():
         extra["sweep_24x16"] = batch_sweep(P, torch)
         extra["prefill_longctx"] = prefill_longctx(P, torch)
         extra["synthetic_error"] = synthetic_error_study(P, torch)
+        extra["pace4_shared_keys_b64"] = shared_key_heads(P, torch, peak)
 
     cb = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:

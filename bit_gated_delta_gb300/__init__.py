@@ -27,9 +27,9 @@ __all__ = [
 
 def make_config(n_heads: int, d: int, max_batch: int, dP: int = 8, group: int = 64, zero_point: int = 0,
                 buf_mode: int = PACE_BUF_INT8, state_mode: int = PACE_STATE_QUANT, io_dtype: int = PACE_IO_BF16,
-                prefill_chunk: int = 256) -> pace_config:
+                prefill_chunk: int = 256, key_heads: int = 0) -> pace_config:
     return pace_config(n_heads, d, d, max_batch, dP, group, zero_point, buf_mode, state_mode, prefill_chunk,
-                       io_dtype)
+                       io_dtype, key_heads)
 
 
 def _ptr(x):

@@ -23,7 +23,7 @@ _STATUS_NAMES = {0: "PACE_OK", 1: "PACE_ERR_INVALID_ARG", 2: "PACE_ERR_UNSUPPORT
 class pace_config(C.Structure):
     _fields_ = [("n_heads", C.c_int), ("d_k", C.c_int), ("d_v", C.c_int), ("max_batch", C.c_int),
                 ("dP", C.c_int), ("group", C.c_int), ("zero_point", C.c_int), ("buf_mode", C.c_int),
-                ("state_mode", C.c_int), ("prefill_chunk", C.c_int), ("io_dtype", C.c_int)]
+                ("state_mode", C.c_int), ("prefill_chunk", C.c_int), ("io_dtype", C.c_int), ("key_heads", C.c_int)]
 
 
 class pace_layout(C.Structure):

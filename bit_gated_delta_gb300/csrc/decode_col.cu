@@ -519,7 +519,8 @@ static cudaError_t launch_col_t(const PaceDev &d, const PaceIO &io, int has_toke
 
 // The int4 pool of a state with d = 128, an int8 buffer and dP <= 8 (the PACE-4 and PACE-4/8 int4 heads).
 bool pace_decode_col_supported(const PaceDev &d) {
-  return d.D == 128 && d.buf_mode == PACE_BUF_INT8 && d.dP <= pace::dcol::MAXP && d.state_mode == PACE_STATE_QUANT;
+  return d.D == 128 && d.buf_mode == PACE_BUF_INT8 && d.dP <= pace::dcol::MAXP && d.state_mode == PACE_STATE_QUANT &&
+         d.gamma == 1;
 }
 
 cudaError_t pace_launch_decode_col(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {

@@ -229,6 +229,17 @@ __device__ __forceinline__ float rcp_bf16(float s) {
   return __uint_as_float(__float_as_uint(__ldg(&g_rcp.v[(b >> 16) & 0x7Fu])) + ((127u - e) << 23));
 }
 
+// Key head of unit u = b*H + h: value head h reads key head h / gamma (q, k and the buffered key codes); the first
+// value head of each key head writes the shared buffer row (all of them compute the same codes).
+__device__ __forceinline__ int key_unit(const PaceDev &st, int unit) {
+  if (st.gamma == 1) return unit;
+  const int b = unit / st.H;
+  return b * st.Hk + (unit - b * st.H) / st.gamma;
+}
+__device__ __forceinline__ bool key_writer(const PaceDev &st, int unit) {
+  return st.gamma == 1 || (unit % st.H) % st.gamma == 0;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -301,7 +312,7 @@ __device__ __forceinline__ void dm_issue_rows(const PaceDev &st, int unit, int n
   const int lane = threadIdx.x & 31, dP = st.dP;
   const int rk = mixed ? D / 2 : D, rv = mixed ? 2 * D : D;
   unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
-  const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
+  const char *gk = static_cast<const char *>(st.buf_k) + (size_t)key_unit(st, unit) * dP * rk;
   const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
   for (int c = lane; c < n * rk / 16; c += 32) cp_async16(kdst + 16 * c, gk + 16 * c);
   for (int c = lane; c < n * rv / 16; c += 32) cp_async16(sh.vrow + 16 * c, gv + 16 * c);
@@ -324,10 +335,10 @@ __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, in
   for (int c = 0; c < CPL; ++c) tin.kx[c] = tin.vx[c] = tin.qx[c] = 0.0f;
   tin.an = tin.bn = 0.0f;
   if (has_token) {
-    const size_t e0 = (size_t)unit * D + CPL * lane;
-    dm_load_io<CPL>(io.k, e0, st.io, tin.kx);
+    const size_t e0 = (size_t)unit * D + CPL * lane, ek = (size_t)key_unit(st, unit) * D + CPL * lane;
+    dm_load_io<CPL>(io.k, ek, st.io, tin.kx);
     dm_load_io<CPL>(io.v, e0, st.io, tin.vx);
-    dm_load_io<CPL>(io.q, e0, st.io, tin.qx);
+    dm_load_io<CPL>(io.q, ek, st.io, tin.qx);
     tin.an = io.a[unit];
     tin.bn = io.beta[unit];
   }
@@ -396,10 +407,14 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
     for (int c = 0; c < CPL; ++c) ck[c] = min(max(__float2int_rn(__fmul_rn(kx[c], rkk)), -qk), qk);
     dm_store_bytes<CPL>(sh.krow + m0 * D + col0, ck);
     float sv = 0.0f;
+    const size_t ku = key_unit(st, unit);
+    const bool kw = key_writer(st, unit);
     if (mixed) {
-      uint8_t *bk = static_cast<uint8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * (D / 2) + col0 / 2;
+      uint8_t *bk = static_cast<uint8_t *>(st.buf_k) + (ku * dP + m0) * (D / 2) + col0 / 2;
+      if (kw) {
 #pragma unroll
-      for (int c = 0; c < CPL; c += 2) bk[c / 2] = (uint8_t)((ck[c] + 8) | ((ck[c + 1] + 8) << 4));
+        for (int c = 0; c < CPL; c += 2) bk[c / 2] = (uint8_t)((ck[c] + 8) | ((ck[c + 1] + 8) << 4));
+      }
       __nv_bfloat16 *bv = static_cast<__nv_bfloat16 *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0;
       uint32_t *vr = reinterpret_cast<uint32_t *>(sh.vrow + ((size_t)m0 * D + col0) * 2);
 #pragma unroll
@@ -415,7 +430,7 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
       int cv[CPL];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) cv[c] = min(max(__float2int_rn(__fmul_rn(vx[c], rvv)), -127), 127);
-      dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * D + col0, ck);
+      if (kw) dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + (ku * dP + m0) * D + col0, ck);
       dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0, cv);
       dm_store_bytes<CPL>(sh.vrow + m0 * D + col0, cv);
     }
@@ -977,7 +992,7 @@ __device__ __forceinline__ void dc_issue(const PaceDev &st, const PaceIO &io, in
   const int rk = MX ? D / 2 : D, rv = MX ? 2 * D : D;
   if (warp == 0) {
     unsigned char *kdst = MX ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
-    const char *gk = static_cast<const char *>(st.buf_k) + (size_t)unit * dP * rk;
+    const char *gk = static_cast<const char *>(st.buf_k) + (size_t)key_unit(st, unit) * dP * rk;
     for (int c = lane; c < dP * rk / 16; c += 32) cp_async16(kdst + 16 * c, gk + 16 * c);
   } else if (warp == 1) {
     const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
@@ -988,9 +1003,9 @@ __device__ __forceinline__ void dc_issue(const PaceDev &st, const PaceIO &io, in
   an = bn = 0.0f;
   bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (has_token) {
-    const size_t e0 = (size_t)unit * D + CPL * lane;
-    if (warp < 2) dm_load_io<CPL>(warp == 0 ? io.k : io.v, e0, st.io, x);
-    if (warp == 0) dm_load_io<CPL>(io.q, e0, st.io, xq);
+    const size_t e0 = (size_t)unit * D + CPL * lane, ek = (size_t)key_unit(st, unit) * D + CPL * lane;
+    if (warp < 2) dm_load_io<CPL>(warp == 0 ? io.k : io.v, warp == 0 ? ek : e0, st.io, x);
+    if (warp == 0) dm_load_io<CPL>(io.q, ek, st.io, xq);
     an = io.a[unit];
     bn = io.beta[unit];
   }
@@ -1036,12 +1051,15 @@ __device__ void dc_stage(const PaceDev &st, int unit, int m0, int has_token, con
 #pragma unroll
       for (int c = 0; c < CPL; ++c) ck[c] = min(max(__float2int_rn(__fmul_rn(x[c], rkk)), -qk), qk);
       dm_store_bytes<CPL>(sh.krow + m0 * D + col0, ck);
-      if (MX) {
-        uint8_t *bk = static_cast<uint8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * (D / 2) + col0 / 2;
+      const size_t ku = key_unit(st, unit);
+      if (key_writer(st, unit)) {
+        if (MX) {
+          uint8_t *bk = static_cast<uint8_t *>(st.buf_k) + (ku * dP + m0) * (D / 2) + col0 / 2;
 #pragma unroll
-        for (int c = 0; c < CPL; c += 2) bk[c / 2] = (uint8_t)((ck[c] + 8) | ((ck[c + 1] + 8) << 4));
-      } else {
-        dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + ((size_t)unit * dP + m0) * D + col0, ck);
+          for (int c = 0; c < CPL; c += 2) bk[c / 2] = (uint8_t)((ck[c] + 8) | ((ck[c + 1] + 8) << 4));
+        } else {
+          dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + (ku * dP + m0) * D + col0, ck);
+        }
       }
       if (lane == 0) {
         float *e = st.buf_s + ((size_t)unit * dP + m0) * 4;

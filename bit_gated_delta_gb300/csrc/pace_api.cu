@@ -52,6 +52,10 @@ pace_status validate_config(const pace_config *c, const uint8_t *mask) {
   if (c->prefill_chunk != 256)
     return fail(PACE_ERR_UNSUPPORTED, "prefill_chunk %d: the method fixes it to 256", c->prefill_chunk);
   if (c->io_dtype != PACE_IO_BF16 && c->io_dtype != PACE_IO_F32) return fail(PACE_ERR_INVALID_ARG, "bad io_dtype");
+  if (c->key_heads < 0 || (c->key_heads > 0 && c->n_heads % c->key_heads))
+    return fail(PACE_ERR_INVALID_ARG, "key_heads %d does not divide n_heads %d", c->key_heads, c->n_heads);
+  if (c->key_heads > 0 && c->key_heads != c->n_heads && c->state_mode != PACE_STATE_QUANT)
+    return fail(PACE_ERR_UNSUPPORTED, "shared key heads need the quantized state mode");
   switch (c->state_mode) {
     case PACE_STATE_QUANT:
       if (c->buf_mode != PACE_BUF_INT8 && c->buf_mode != PACE_BUF_MIXED)
@@ -82,6 +86,7 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
   const size_t none = (size_t)-1;
   L.codes4 = L.codes8 = L.scale = L.zp = L.buf_k = L.buf_v = L.buf_s = L.m = L.S = L.status = none;
   const size_t B = (size_t)batch, H = (size_t)c->n_heads, D = (size_t)c->d_k, NG = D / (size_t)c->group;
+  const size_t Hk = c->key_heads > 0 ? (size_t)c->key_heads : H;
   const size_t P = (size_t)c->dP;
   int h4 = 0, h8 = 0;
   for (int h = 0; h < c->n_heads; ++h) {
@@ -102,10 +107,10 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
     take(L.scale, B * H * NG * D * 2);
     if (c->zero_point) take(L.zp, B * H * NG * D);
     if (c->buf_mode == PACE_BUF_MIXED) {
-      take(L.buf_k, B * H * P * (D / 2));
+      take(L.buf_k, B * Hk * P * (D / 2));
       take(L.buf_v, B * H * P * D * 2);
     } else {
-      take(L.buf_k, B * H * P * D);
+      take(L.buf_k, B * Hk * P * D);
       take(L.buf_v, B * H * P * D);
     }
     take(L.buf_s, B * H * P * 16);
@@ -192,6 +197,8 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
   d.io = cfg->io_dtype;
   d.H4 = L.H4;
   d.H8 = L.H8;
+  d.Hk = cfg->key_heads > 0 ? cfg->key_heads : cfg->n_heads;
+  d.gamma = cfg->n_heads / d.Hk;
   d.codes4 = at<uint32_t>(s->base, L.codes4);
   d.codes8 = at<uint32_t>(s->base, L.codes8);
   d.scale = at<__nv_bfloat16>(s->base, L.scale);
@@ -405,7 +412,8 @@ double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, i
   const double f8 = n8 / H;
   auto payload = [&](int bits) { return bits + (16.0 + (cfg->zero_point ? bits : 0)) / cfg->group; };
   const double bk = cfg->buf_mode == PACE_BUF_MIXED ? 4.0 : 8.0, bv = cfg->buf_mode == PACE_BUF_MIXED ? 16.0 : 8.0;
-  const double c = (bk * D + bv * D + 32.0) / (D * D);
+  const double gamma = cfg->key_heads > 0 ? H / cfg->key_heads : 1.0;
+  const double c = (bk * D / gamma + bv * D + 32.0) / (D * D);
   return (1.0 - f8) * payload(4) + f8 * payload(8) + c * cfg->dP;
 }
 

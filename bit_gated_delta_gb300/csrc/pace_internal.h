@@ -12,6 +12,7 @@ struct PaceDev {
   int B, H, D, G, NG, dP;
   int zero_point, buf_mode, state_mode, io;
   int H4, H8;
+  int Hk, gamma;           // key heads; value heads per key head (value head h reads key head h / gamma)
   uint32_t *codes4;        // [B][H4][D/8][D]
   uint32_t *codes8;        // [B][H8][D/4][D]
   __nv_bfloat16 *scale;    // [B][H][NG][D]

@@ -89,8 +89,9 @@ __global__ void __launch_bounds__(D) prefill_kernel(const PaceDev st, const Pace
   for (int t0 = 0; t0 < n; t0 += PF_STAGE) {
     const int nt = min(PF_STAGE, n - t0);
     __syncthreads();
+    const long kunit = (unit / st.H) * st.Hk + (unit % st.H) / st.gamma;   // key head of this value head
     for (int tt = 0; tt < nt; ++tt) {
-      const long row = (unit * n + t0 + tt) * D + j;
+      const long row = (kunit * n + t0 + tt) * D + j;
       k_s[tt * D + j] = load_io(io.k, row, st.io);
       q_s[tt * D + j] = load_io(io.q, row, st.io);
     }

@@ -200,13 +200,14 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
 
   // the k, q rows (K-major cores) and v rows of the sub-chunk starting at token s0, as asynchronous copies;
   // padding tokens (s0 + t >= n) are zeros
+  const long kunit = (unit / st.H) * st.Hk + (unit % st.H) / st.gamma;   // key head of this value head
   auto issue_rows = [&](int s0) {
     const int ns = min(T, n - s0);
 #pragma unroll
     for (int it = 0; it < 8; ++it) {                    // 64 rows x 16 chunks of 16 bytes
       const int c = tid + NT * it, row = c >> 4, c8 = c & 15, t = row & (T - 1);
       const bool in = t < ns;
-      const __nv_bfloat16 *src = (row < T ? gk : gq) + ((unit * n + s0 + (in ? t : 0)) * D + 8 * c8);
+      const __nv_bfloat16 *src = (row < T ? gk : gq) + ((kunit * n + s0 + (in ? t : 0)) * D + 8 * c8);
       cp16_zfill(smem + OFF_X + core_off(row, 8 * c8, D), src, in ? 16u : 0u);
     }
 #pragma unroll

@@ -17,8 +17,9 @@
  *   - Calls enqueue work on `stream` and return without synchronising. Argument errors are detected on
  *     the host and returned before anything is launched; a failed launch returns PACE_ERR_CUDA.
  *     pace_last_error() gives a message for the last failure of the calling thread.
- *   - q, k [B, H, d_k], v and o [B, H, d_v] (decode) or [B, H, n, d] (prefill) are dense row-major
- *     tensors of the configured I/O type (bf16 or fp32); a and beta are fp32 [B, H] or [B, H, n].
+ *   - q, k [B, H_k, d_k], v and o [B, H, d_v] (decode) or [B, H_k | H, n, d] (prefill) are dense row-major
+ *     tensors of the configured I/O type (bf16 or fp32), H_k = key heads (= H unless configured); a and beta
+ *     are fp32 [B, H] or [B, H, n].
  *   - The library does not L2-normalise k, does not scale q, and applies no output gate or norm.
  *   - Calls on one state must not overlap on the GPU (same stream, or ordered by events).
  */
@@ -70,6 +71,9 @@ typedef struct {
   int state_mode;     /* PACE_STATE_* */
   int prefill_chunk;  /* tokens rounded together in prefill; must be 256 ([P1] 어떻게 동작하나) */
   int io_dtype;       /* PACE_IO_* for q, k, v, o */
+  int key_heads;      /* key heads H_k (0 = n_heads): gamma = n_heads / key_heads value heads share one key head,
+                         its q and k, and one copy of its buffered key codes ([P1] 어떻게 동작하나: the buffer term
+                         b_k d_k / gamma). gamma > 1 needs PACE_STATE_QUANT; value head h uses key head h / gamma */
 } pace_config;
 
 typedef struct pace_state pace_state;   /* opaque host handle */
@@ -87,7 +91,7 @@ typedef struct pace_state pace_state;   /* opaque host handle */
  *           zero-point codes are stored as they are
  *   scale   bf16   [B][H][d_k/g][d_v]   group scales
  *   zp      uint8  [B][H][d_k/g][d_v]   zero points (zero-point mode)
- *   buf_k   int8   [B][H][dP][d_k]      int8 buffer; mixed: uint8 [B][H][dP][d_k/2], key 2t in the low
+ *   buf_k   int8   [B][H_k][dP][d_k]    int8 buffer (one row per key head); mixed: uint8 [B][H_k][dP][d_k/2], key 2t in the low
  *                                      nibble of byte t, 2t+1 in the high one, stored as code+8;
  *                                      fp32 buffer: float [B][H][dP][d_k]
  *   buf_v   int8   [B][H][dP][d_v]      mixed: bf16 values; fp32 buffer: float
@@ -169,7 +173,7 @@ pace_status pace_state_import(pace_state *state, const void *src, size_t bytes, 
 
 /* Resident bits per state value ([P1] 어떻게 동작하나, 무엇과 다른가). literal_formula != 0: payload
  * b + (16 + zero-point bits)/g averaged over heads, plus the buffer cost c*dP with
- * c = (b_k d_k + b_v d_v + 32)/(d_k d_v) (one value head per key head); literal_formula == 0: the bytes
+ * c = (b_k d_k / gamma + b_v d_v + 32)/(d_k d_v), gamma = value heads per key head; literal_formula == 0: the bytes
  * this library actually keeps per state value (codes, scales, zero points, buffer, counters) * 8.
  * head_is_int8 as for pace_state_bytes. Returns a negative value for an invalid config. */
 double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, int literal_formula);

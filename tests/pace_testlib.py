@@ -142,7 +142,7 @@ class PairRun:
     """
 
     def __init__(self, wl: synth.Workload, state_mode: int = 0, mask=None, sample=None, dP=None, layer=0,
-                 out_f32: bool = False):
+                 out_f32: bool = False, key_heads: int = 0):
         import torch
         import bit_gated_delta_gb300 as P
         self.P, self.torch = P, torch
@@ -162,7 +162,10 @@ class PairRun:
         self.io_bf16 = wl.io == "bf16" and not out_f32
         self.cfg = P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, zero_point=wl.zero_point, buf_mode=buf,
                                  state_mode=state_mode,
-                                 io_dtype=P.PACE_IO_BF16 if self.io_bf16 else P.PACE_IO_F32)
+                                 io_dtype=P.PACE_IO_BF16 if self.io_bf16 else P.PACE_IO_F32, key_heads=key_heads)
+        # shared key heads: value head h reads the q and k of key head h // gamma (here: of value head
+        # gamma * (h // gamma)); the library gets the [B, H_k, ...] tensors, the oracle each head's copy
+        self.gamma = wl.H // key_heads if key_heads else 1
         self.state = P.PaceState(self.cfg, wl.B, self.mask if state_mode == 0 else None)
         self.sample = sample if sample is not None else [(b, h) for b in range(wl.B) for h in range(wl.H)]
         om = {0: O.STATE_QUANT, 1: O.STATE_FP32, 2: O.STATE_BF16, 3: O.STATE_BF16_BUF}[state_mode]
@@ -189,12 +192,21 @@ class PairRun:
             return e <= tol, f"rel_l2 {e:.3e}"
         return bf16_within_ulp(got, ref)
 
+    def _share_keys(self, x):
+        if self.gamma == 1:
+            return x, x["q"], x["k"]
+        x = dict(x)
+        for key in ("q", "k"):
+            x[key] = np.repeat(x[key][:, ::self.gamma], self.gamma, axis=1)
+        return x, np.ascontiguousarray(x["q"][:, ::self.gamma]), np.ascontiguousarray(x["k"][:, ::self.gamma])
+
     def prefill(self, n: int, inputs=None):
         wl = self.wl
         x = inputs if inputs is not None else synth.chunk_inputs(wl, self.t, n, self.layer)
+        x, qg, kg = self._share_keys(x)
         o = self.torch.empty(wl.B, wl.H, n, wl.d_v, device="cuda",
                              dtype=self.torch.bfloat16 if self.io_bf16 else self.torch.float32)
-        self.state.prefill_chunk(self._dev(x["q"], True), self._dev(x["k"], True), self._dev(x["v"], True),
+        self.state.prefill_chunk(self._dev(qg, True), self._dev(kg, True), self._dev(x["v"], True),
                                  self._dev(x["a"], False), self._dev(x["beta"], False), o)
         got = o.float().cpu().numpy()
         refs, gots = [], []
@@ -209,9 +221,10 @@ class PairRun:
     def decode(self, inputs=None):
         wl = self.wl
         x = inputs if inputs is not None else synth.token_inputs(wl, self.t, self.layer)
+        x, qg, kg = self._share_keys(x)
         o = self.torch.empty(wl.B, wl.H, wl.d_v, device="cuda",
                              dtype=self.torch.bfloat16 if self.io_bf16 else self.torch.float32)
-        self.state.decode_step(self._dev(x["q"], True), self._dev(x["k"], True), self._dev(x["v"], True),
+        self.state.decode_step(self._dev(qg, True), self._dev(kg, True), self._dev(x["v"], True),
                                self._dev(x["a"], False), self._dev(x["beta"], False), o)
         got = o.float().cpu().numpy()
         refs, gots = [], []

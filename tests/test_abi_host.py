@@ -108,17 +108,22 @@ def test_assign_heads_matches_oracle(P):
         P.pace_assign_heads(np.ones(4), np.full(4, 0.9), 8, 1.5)
 
 
-@pytest.mark.parametrize("zp,g,buf,n8", [(0, 64, 0, 0), (1, 32, 1, 8), (1, 32, 0, 8), (0, 32, 0, 0)])
-def test_resident_bits_formula_matches_oracle_accounting(P, zp, g, buf, n8):
+@pytest.mark.parametrize("zp,g,buf,n8,kh", [(0, 64, 0, 0, 32), (1, 32, 1, 8, 32), (1, 32, 0, 8, 32), (0, 32, 0, 0, 32),
+                                             (0, 64, 0, 0, 16), (1, 32, 1, 8, 8)])
+def test_resident_bits_formula_matches_oracle_accounting(P, zp, g, buf, n8, kh):
     H, D, dP = 32, 128, 8
     mask = np.zeros(H, np.uint8)
     mask[:n8] = 1
-    cfg = P.make_config(H, D, 16, dP=dP, group=g, zero_point=zp, buf_mode=buf)
+    cfg = P.make_config(H, D, 16, dP=dP, group=g, zero_point=zp, buf_mode=buf, key_heads=kh)
     got = P.pace_resident_bits(cfg, mask, True)
     f8 = n8 / H
     payload = (1 - f8) * O.payload_bits(4, g, zp) + f8 * O.payload_bits(8, g, zp)
     bk, bv = (4, 16) if buf == 1 else (8, 8)
-    ref = payload + O.buffer_bits(D, D, bk, bv, 1.0, 32, dP)
+    ref = payload + O.buffer_bits(D, D, bk, bv, H / kh, 32, dP)
     assert got == pytest.approx(ref, rel=1e-12)
     exact = P.pace_resident_bits(cfg, mask, False)
     assert exact >= got - 1e-9     # the layout keeps beta and per-token scales too
+    if kh < H:                     # shared key heads keep one buffered key row per key head
+        full = P.pace_resident_bits(P.make_config(H, D, 16, dP=dP, group=g, zero_point=zp, buf_mode=buf), mask, False)
+        kbytes = (0.5 if buf == 1 else 1.0) * D * dP * 16 * (H - kh)
+        assert full - exact == pytest.approx(8.0 * kbytes / (16 * H * D * D), rel=1e-3, abs=1e-3)
