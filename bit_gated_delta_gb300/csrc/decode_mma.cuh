@@ -36,9 +36,14 @@ constexpr int DM_WARPS = 4;   // units (warps) per block
 #ifndef PACE_DM_CTA_PER_UNIT
 #define PACE_DM_CTA_PER_UNIT 0  // 1: the CTA-per-unit kernel at every batch size
 #endif
-#ifndef PACE_DM_MIN_BLOCKS
-#define PACE_DM_MIN_BLOCKS 4  // resident blocks per SM the int4 kernels are compiled for (register cap)
+#ifndef PACE_DM_UNITS_PER_BLOCK
+#define PACE_DM_UNITS_PER_BLOCK 1  // warps (units) per block of the warp-per-unit kernel
 #endif
+#ifndef PACE_DM_MIN_WARPS
+#define PACE_DM_MIN_WARPS 16  // resident warps per SM the int4 kernels are compiled for (register cap)
+#endif
+constexpr int DM_UPB = PACE_DM_UNITS_PER_BLOCK;
+static_assert(PACE_DM_MIN_WARPS % DM_UPB == 0 && 12 % DM_UPB == 0, "units per block must divide the warps per SM");
 constexpr int PB_STRIDE = 40; // floats per row of the per-block dot table (conflict-free fragment stores)
 constexpr int UB_STRIDE = 36; // floats per row of the per-block replay table (conflict-free fragment loads)
 
@@ -920,20 +925,28 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
   uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
 
-  // everything that does not depend on the buffer count is in flight before the count is read: the unit's
-  // code words (into L2, and the first column block into registers), scales, zero points, the new token
-  if (lane == 0) prefetch_l2(codes, PL * PLANE * 4);
-  uint32_t cw[PL][2][NPP][4];
-  dm_load_block<D, PL>(codes, 0, lane, cw);
+  // The loads on the path to the first dot product go out first, in the order they are needed: the buffer
+  // count (it gates the buffered rows), the new token, scales and zero points, the first column block's words;
+  // then, once the count is known, the buffered rows; only then the L2 prefetch of the other blocks, so that
+  // the bulk of the state does not queue ahead of the staging loads.
+  const int m0 = st.m[unit];
   TokenIn<D / 32> tin;
   dm_issue<D, G, ZP, MX>(st, io, unit, has_token, sh, tin);
-  const int m0 = st.m[unit];
+  uint32_t cw[PL][2][NPP][4];
+  dm_load_block<D, PL>(codes, 0, lane, cw);
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
     cp_async_wait_all();                         // nothing may land in shared memory after the warp leaves
     if (has_token && m0 != 0)                    // corrupted counter: leave the unit, emit zeros
       for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
     return;                                      // (or a flush with nothing pending)
   }
+  if (m0 > 0) {
+    dm_issue_rows<D, MX>(st, unit, m0, sh);
+    if (lane < m0) tin.bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
+    tin.pre = m0;
+  }
+  constexpr uint32_t BLK = 2 * NPP * 128;        // words of one 32-column block in a plane
+  if (lane < PL) prefetch_l2(codes + lane * PLANE + BLK, (PLANE - BLK) * 4);
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
   const int nv = mt + (has_token ? 3 : 0);
@@ -955,11 +968,11 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 // (int4: 16 warps per SM at <= 128 registers; int8, with twice the code words live: 12 warps per SM).
 // Warp w of the launch handles pool unit w: sequence w / HP, the pool's head slot w % HP.
 template <int D, int G, int BITS, int ZP, int MX>
-__global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? PACE_DM_MIN_BLOCKS : 3) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+__global__ void __launch_bounds__(DM_UPB * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : 12) / DM_UPB) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int HP = BITS == 4 ? st.H4 : st.H8;
-  const int w = blockIdx.x * DM_WARPS + warp;
+  const int w = blockIdx.x * DM_UPB + warp;
   if (w >= st.B * HP) return;
   const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
@@ -1315,8 +1328,9 @@ static int dm_sm_count() {
 }
 
 template <int D, int G, int BITS, int ZP, int MX>
-static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, size_t smem) {
+static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, size_t unit_smem) {
   static size_t opted = 0;
+  const size_t smem = (size_t)DM_WARPS * unit_smem;   // the larger of the two launch shapes
   if (smem > 48 * 1024 && smem > opted) {
     cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
@@ -1330,8 +1344,9 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
   if (PACE_DM_CTA_PER_UNIT || units * DM_WARPS <= (long)dm_sm_count() * 16) {
     decode_split_kernel<D, G, BITS, ZP, MX><<<(unsigned)units, DM_WARPS * 32, smem, s>>>(d, io, has_token);
   } else {
-    const long blocks = (units + DM_WARPS - 1) / DM_WARPS;
-    decode_mma_kernel<D, G, BITS, ZP, MX><<<(unsigned)blocks, DM_WARPS * 32, smem, s>>>(d, io, has_token);
+    // small blocks, so that the units spread evenly over the SMs (the slowest SM sets the step time)
+    const long blocks = (units + DM_UPB - 1) / DM_UPB;
+    decode_mma_kernel<D, G, BITS, ZP, MX><<<(unsigned)blocks, DM_UPB * 32, (size_t)DM_UPB * unit_smem, s>>>(d, io, has_token);
   }
   return cudaGetLastError();
 }
@@ -1339,10 +1354,9 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
 template <int D, int G, int ZP, int MX>
 static cudaError_t launch_mma_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, bool int4_pool = true) {
   const MmaSmem L = mma_smem(D, G, d.dP, MX, ZP);
-  const size_t smem = (size_t)DM_WARPS * L.total;
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = int4_pool ? launch_pool<D, G, 4, ZP, MX>(d, io, has_token, s, smem) : cudaSuccess;
-  if (e == cudaSuccess) e = launch_pool<D, G, 8, ZP, MX>(d, io, has_token, s, smem);
+  if ((size_t)DM_WARPS * L.total > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = int4_pool ? launch_pool<D, G, 4, ZP, MX>(d, io, has_token, s, L.total) : cudaSuccess;
+  if (e == cudaSuccess) e = launch_pool<D, G, 8, ZP, MX>(d, io, has_token, s, L.total);
   return e;
 }
 
