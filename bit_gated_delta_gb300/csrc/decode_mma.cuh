@@ -323,12 +323,10 @@ __device__ __forceinline__ void dm_issue_rows(const PaceDev &st, int unit, int n
   for (int c = lane; c < n * rv / 16; c += 32) cp_async16(sh.vrow + 16 * c, gv + 16 * c);
 }
 
-// Loads of a unit that do not depend on its buffer count: the scales and zero points (asynchronous copies
-// into shared memory) and the new token (registers).
-template <int D, int G, int ZP, int MX>
-__device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, int unit, int has_token,
-                                         const MmaShared &sh, TokenIn<D / 32> &tin, int pre = 0) {
-  constexpr int CPL = D / 32, NG = D / G;
+// The unit's group scales and zero points, as asynchronous copies into shared memory.
+template <int D, int G, int ZP>
+__device__ __forceinline__ void dm_issue_scales(const PaceDev &st, int unit, const MmaShared &sh) {
+  constexpr int NG = D / G;
   const int lane = threadIdx.x & 31;
   const char *gs = reinterpret_cast<const char *>(st.scale + (size_t)unit * NG * D);
   for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(sh.ssc) + 16 * c, gs + 16 * c);
@@ -336,6 +334,14 @@ __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, in
     const char *gz = reinterpret_cast<const char *>(st.zp + (size_t)unit * NG * D);
     for (int c = lane; c < NG * D / 16; c += 32) cp_async16(sh.szp + 16 * c, gz + 16 * c);
   }
+}
+
+// The new token of the step into registers (zeros without one).
+template <int D>
+__device__ __forceinline__ void dm_load_token(const PaceDev &st, const PaceIO &io, int unit, int has_token,
+                                              TokenIn<D / 32> &tin) {
+  constexpr int CPL = D / 32;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int c = 0; c < CPL; ++c) tin.kx[c] = tin.vx[c] = tin.qx[c] = 0.0f;
   tin.an = tin.bn = 0.0f;
@@ -347,12 +353,8 @@ __device__ __forceinline__ void dm_issue(const PaceDev &st, const PaceIO &io, in
     tin.an = io.a[unit];
     tin.bn = io.beta[unit];
   }
-  tin.pre = pre;
+  tin.pre = 0;
   tin.bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (pre > 0) {                                 // small batches: every buffered row, before the count is known
-    dm_issue_rows<D, MX>(st, unit, pre, sh);
-    if (lane < pre) tin.bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * st.dP + lane) * 4);
-  }
 }
 
 // Stage the unit: the buffered tokens (asynchronous copies, all in flight at once: int8 keys straight into
@@ -369,7 +371,6 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
   const int mt = m0 + has_token;
   constexpr int mixed = MX;
   unsigned char *kdst = mixed ? reinterpret_cast<unsigned char *>(sh.ah) : reinterpret_cast<unsigned char *>(sh.krow);
-  if (tin.pre == 0 && m0 > 0) dm_issue_rows<D, MX>(st, unit, m0, sh);
   float sa = 0.0f, sb = 0.0f, ssk = 0.0f, ssv = 0.0f;
   if (lane < m0) {
     const float4 r = tin.pre ? tin.bs : *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
@@ -377,22 +378,6 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
   }
   const float *kx = tin.kx, *vx = tin.vx, *qx = tin.qx;
   const float an = tin.an, bn = tin.bn;
-  cp_async_wait_all();
-  __syncwarp();
-  if (mixed) {
-    for (int t = 0; t < m0; ++t) {
-      if (lane < D / 8) {                       // one 8-key run per lane: nibble code + 8 -> int8
-        const uint32_t nb = *reinterpret_cast<const uint32_t *>(kdst + t * (D / 2) + 4 * lane);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          lo |= (uint32_t)(((int)((nb >> (8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
-          hi |= (uint32_t)(((int)((nb >> (16 + 8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
-        }
-        *reinterpret_cast<uint2 *>(sh.krow + t * D + 8 * lane) = make_uint2(lo, hi);
-      }
-    }
-  }
   if (has_token) {
     float mk = 0.0f, mv = 0.0f, mq = 0.0f;
 #pragma unroll
@@ -467,24 +452,66 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
       sh.vsc[mt + 2] = sigma;
     }
   }
+  // the buffered rows have landed (the new token's rows above are other slots)
+  cp_async_wait_all();
+  __syncwarp();
+  if (mixed) {
+    for (int t = 0; t < m0; ++t) {
+      if (lane < D / 8) {                       // one 8-key run per lane: nibble code + 8 -> int8
+        const uint32_t nb = *reinterpret_cast<const uint32_t *>(kdst + t * (D / 2) + 4 * lane);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          lo |= (uint32_t)(((int)((nb >> (8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
+          hi |= (uint32_t)(((int)((nb >> (16 + 8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
+        }
+        *reinterpret_cast<uint2 *>(sh.krow + t * D + 8 * lane) = make_uint2(lo, hi);
+      }
+    }
+  }
   if (lane < mt) {
     sh.a[lane] = sa;
     sh.vsc[lane] = ssk;
   }
   bt = sb;
   sv_out = ssv;
-  __syncwarp();
-  if (lane < mt) {
-    const int ws = dm_wstride(dP);
-    float g = 1.0f, dm = 1.0f;
-    for (int r = 0; r <= lane; ++r) g *= sh.a[r];
-    for (int r = lane + 1; r < mt; ++r) dm *= sh.a[r];
-    sh.gam[lane] = g;
-    sh.dmq[lane] = dm;
-    float p = 1.0f;                             // G_t/G_s = a_{s+1} .. a_t for t = lane, s < t
-    for (int s = lane - 1; s >= 0; --s) {
-      p *= sh.a[s + 1];
-      sh.dmt[lane * ws + s] = p;
+  const int ws = dm_wstride(dP);
+  if (dP <= 8) {                                // a_t of every token in registers: fixed-length products
+    float ar[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) ar[r] = __shfl_sync(0xffffffffu, sa, r);
+    if (lane < mt) {
+      float g = 1.0f, dm = 1.0f;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r <= lane) g *= ar[r];
+        if (r > lane && r < mt) dm *= ar[r];
+      }
+      sh.gam[lane] = g;
+      sh.dmq[lane] = dm;
+      float p = 1.0f;                           // G_t/G_s = a_{s+1} .. a_t for t = lane, s < t
+#pragma unroll
+      for (int s = 6; s >= 0; --s) {
+        if (s < lane) {
+          p *= ar[s + 1];
+          sh.dmt[lane * ws + s] = p;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    __syncwarp();
+    if (lane < mt) {
+      float g = 1.0f, dm = 1.0f;
+      for (int r = 0; r <= lane; ++r) g *= sh.a[r];
+      for (int r = lane + 1; r < mt; ++r) dm *= sh.a[r];
+      sh.gam[lane] = g;
+      sh.dmq[lane] = dm;
+      float p = 1.0f;
+      for (int s = lane - 1; s >= 0; --s) {
+        p *= sh.a[s + 1];
+        sh.dmt[lane * ws + s] = p;
+      }
     }
   }
 }
@@ -499,16 +526,30 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, 
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int nvt = (nv + 15) >> 4;
   const int ws = dm_wstride(dP);
-  for (int idx = lane; idx < 16 * nvt * (D / 8); idx += 32) {   // 8 keys per item
+  auto row_f16 = [&](int idx, uint2 x) {                 // 8 keys per item
     const int row = idx / (D / 8), k8 = 8 * (idx - row * (D / 8));
-    uint4 h = make_uint4(0u, 0u, 0u, 0u);
-    if (row < nv) {
-      const uint2 x = *reinterpret_cast<const uint2 *>(sh.krow + row * D + k8);
-      const bool sx = (k8 & 8) != 0;
-      h = make_uint4(i8pair_f16(x.x, 0x4140, sx), i8pair_f16(x.x, 0x4342, sx), i8pair_f16(x.y, 0x4140, sx),
-                     i8pair_f16(x.y, 0x4342, sx));
-    }
+    const bool sx = (k8 & 8) != 0;
+    const uint4 h = row < nv ? make_uint4(i8pair_f16(x.x, 0x4140, sx), i8pair_f16(x.x, 0x4342, sx),
+                                          i8pair_f16(x.y, 0x4140, sx), i8pair_f16(x.y, 0x4342, sx))
+                             : make_uint4(0u, 0u, 0u, 0u);
     *reinterpret_cast<uint4 *>(sh.ah + ah_off<D>(row, k8 >> 3)) = h;
+  };
+  {                                                      // the first 16 rows: all loads, then all stores
+    constexpr int NIT = 16 * (D / 8) / 32;
+    uint2 x[NIT];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const int idx = lane + 32 * it, row = idx / (D / 8);
+      x[it] = row < nv ? *reinterpret_cast<const uint2 *>(sh.krow + row * D + 8 * (idx - row * (D / 8)))
+                       : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) row_f16(lane + 32 * it, x[it]);
+  }
+  for (int idx = 16 * (D / 8) + lane; idx < 16 * nvt * (D / 8); idx += 32) {
+    const int row = idx / (D / 8);
+    row_f16(idx, row < nv ? *reinterpret_cast<const uint2 *>(sh.krow + row * D + 8 * (idx - row * (D / 8)))
+                          : make_uint2(0u, 0u));
   }
   __syncwarp();
   const int ntg = (mt + 7) >> 3;                 // 8-token tiles of the Gram columns
@@ -516,7 +557,7 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, 
   const int brow = lane & 7, bcol = (lane >> 3) & 1;                       // ldmatrix x2: row, chunk
   for (int vt = 0; vt < nvt; ++vt) {
     float cs[4], gr[4][4];
-#pragma unroll 2
+#pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t a[4];
       ldsm_x4(a, sh.ah + ah_off<D>(16 * vt + arow, 2 * ks + acol));
@@ -925,17 +966,14 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
   uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
 
-  // The loads on the path to the first dot product go out first, in the order they are needed: the buffer
-  // count (it gates the buffered rows), the new token, scales and zero points, the first column block's words;
-  // then, once the count is known, the buffered rows; only then the L2 prefetch of the other blocks, so that
-  // the bulk of the state does not queue ahead of the staging loads.
+  // The loads go out in the order the step needs them: the buffer count (it gates the buffered rows) and the
+  // new token; once the count is known, the buffered rows, then the scales and zero points and the first
+  // column block's words; only then the L2 prefetch of the other blocks, so that the bulk of the state does
+  // not queue ahead of the staging loads.
   const int m0 = st.m[unit];
   TokenIn<D / 32> tin;
-  dm_issue<D, G, ZP, MX>(st, io, unit, has_token, sh, tin);
-  uint32_t cw[PL][2][NPP][4];
-  dm_load_block<D, PL>(codes, 0, lane, cw);
+  dm_load_token<D>(st, io, unit, has_token, tin);
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
-    cp_async_wait_all();                         // nothing may land in shared memory after the warp leaves
     if (has_token && m0 != 0)                    // corrupted counter: leave the unit, emit zeros
       for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
     return;                                      // (or a flush with nothing pending)
@@ -945,6 +983,9 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     if (lane < m0) tin.bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
     tin.pre = m0;
   }
+  dm_issue_scales<D, G, ZP>(st, unit, sh);
+  uint32_t cw[PL][2][NPP][4];
+  dm_load_block<D, PL>(codes, 0, lane, cw);
   constexpr uint32_t BLK = 2 * NPP * 128;        // words of one 32-column block in a plane
   if (lane < PL) prefetch_l2(codes + lane * PLANE + BLK, (PLANE - BLK) * 4);
   const int mt = m0 + has_token;
