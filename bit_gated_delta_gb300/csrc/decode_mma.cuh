@@ -253,22 +253,50 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Global loads issued exactly where they stand in the program (volatile: the compiler neither sinks them past
+// a branch to their first use nor merges them), so that a unit's loads leave in the order the step needs them.
+__device__ __forceinline__ uint32_t ldg_u32(const void *p) {
+  uint32_t r;
+  asm volatile("ld.global.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ldg_v2(const void *p) {
+  uint2 r;
+  asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ldg_v4(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
 
+// CPL consecutive elements (CPL = 2 or 4; the I/O pointers are 16-byte aligned) in one vector load.
 template <int CPL>
 __device__ __forceinline__ void dm_load_io(const void *p, size_t idx, int io, float (&x)[CPL]) {
+  static_assert(CPL == 2 || CPL == 4, "two or four elements per lane");
   if (io == PACE_IO_F32) {
-#pragma unroll
-    for (int e = 0; e < CPL; e += 2) {
-      const float2 v = *reinterpret_cast<const float2 *>(static_cast<const float *>(p) + idx + e);
-      x[e] = v.x;
-      x[e + 1] = v.y;
+    const float *f = static_cast<const float *>(p) + idx;
+    if constexpr (CPL == 4) {
+      const uint4 v = ldg_v4(f);
+      x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y); x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+    } else {
+      const uint2 v = ldg_v2(f);
+      x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
     }
   } else {
+    const __nv_bfloat16 *h = static_cast<const __nv_bfloat16 *>(p) + idx;
+    uint32_t w[CPL / 2];
+    if constexpr (CPL == 4) {
+      const uint2 v = ldg_v2(h);
+      w[0] = v.x; w[1] = v.y;
+    } else {
+      w[0] = ldg_u32(h);
+    }
 #pragma unroll
-    for (int e = 0; e < CPL; e += 2) {
-      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(static_cast<const __nv_bfloat16 *>(p) + idx + e);
-      x[e] = __low2float(v);
-      x[e + 1] = __high2float(v);
+    for (int e = 0; e < CPL / 2; ++e) {
+      x[2 * e] = __uint_as_float(w[e] << 16);
+      x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
     }
   }
 }
@@ -293,7 +321,7 @@ __device__ __forceinline__ void dm_load_block(const uint32_t *codes, int cb, int
     for (int m = 0; m < 2; ++m)
 #pragma unroll
       for (int pp = 0; pp < NPP; ++pp) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(codes + pl * (D * D / 8) + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4);
+        const uint4 v = ldg_v4(codes + pl * (D * D / 8) + (((2 * cb + m) * NPP + pp) * 32 + lane) * 4);
         cw[pl][m][pp][0] = v.x;
         cw[pl][m][pp][1] = v.y;
         cw[pl][m][pp][2] = v.z;
@@ -350,8 +378,8 @@ __device__ __forceinline__ void dm_load_token(const PaceDev &st, const PaceIO &i
     dm_load_io<CPL>(io.k, ek, st.io, tin.kx);
     dm_load_io<CPL>(io.v, e0, st.io, tin.vx);
     dm_load_io<CPL>(io.q, ek, st.io, tin.qx);
-    tin.an = io.a[unit];
-    tin.bn = io.beta[unit];
+    tin.an = __uint_as_float(ldg_u32(io.a + unit));
+    tin.bn = __uint_as_float(ldg_u32(io.beta + unit));
   }
   tin.pre = 0;
   tin.bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -773,17 +801,27 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
       o = gm * (sh.vsc[mt] * sh.pb[mt * PB_STRIDE + lane] +
                 (sh.vsc[mt + 1] * sh.pb[(mt + 1) * PB_STRIDE + lane] + sh.vsc[mt + 2] * sh.pb[(mt + 2) * PB_STRIDE + lane]));
     if (dP <= 8) {                           // u in registers
+      // the per-token operands of every token first (slot min(t, mt - 1) for the unused ones), so that the
+      // chain below waits for shared memory once rather than once per token
+      float pv[8], vv[8], bt[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int tt = min(t, mt - 1);
+        const float4 tk = sh.tk[tt];           // G_t s_kt, beta_t, s_vt, readout coefficient
+        vv[t] = fmaf(-tk.x, sh.pb[tt * PB_STRIDE + lane], value(tt, tk.z));
+        bt[t] = tk.y;
+        pv[t] = tk.w;
+      }
       float u[8];
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
         u[t] = 0.0f;
         if (t < mt) {
-          const float4 tk = sh.tk[t];          // G_t s_kt, beta_t, s_vt, readout coefficient
-          float acc = fmaf(-tk.x, sh.pb[t * PB_STRIDE + lane], value(t, tk.z));
+          float acc = vv[t];
 #pragma unroll
           for (int s2 = 0; s2 < t; ++s2) acc = fmaf(-sh.W[t * 8 + s2], u[s2], acc);
-          u[t] = tk.y * acc;
-          o = fmaf(tk.w, u[t], o);
+          u[t] = bt[t] * acc;
+          o = fmaf(pv[t], u[t], o);
           if (do_flush) sh.ub[t * UB_STRIDE + lane] = u[t];
         }
       }
@@ -970,7 +1008,7 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // new token; once the count is known, the buffered rows, then the scales and zero points and the first
   // column block's words; only then the L2 prefetch of the other blocks, so that the bulk of the state does
   // not queue ahead of the staging loads.
-  const int m0 = st.m[unit];
+  const int m0 = (int)ldg_u32(st.m + unit);
   TokenIn<D / 32> tin;
   dm_load_token<D>(st, io, unit, has_token, tin);
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {

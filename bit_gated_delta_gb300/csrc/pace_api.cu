@@ -243,12 +243,20 @@ pace_status pace_state_get_layout(const pace_state *state, pace_layout *out) {
   return ok();
 }
 
+// The kernels read q, k, v and write o in 8- and 16-byte vectors.
+static bool io_aligned(const void *q, const void *k, const void *v, const float *a, const float *beta, const void *o) {
+  auto al = [](const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+  return al(q, 16) && al(k, 16) && al(v, 16) && al(o, 16) && al(a, 4) && al(beta, 4);
+}
+
 pace_status pace_decode_step(pace_state *state, const void *q, const void *k, const void *v, const float *a,
                              const float *beta, void *o, void *stream) {
   pace_status st = check_state(state);
   if (st != PACE_OK) return st;
   if (!need(q) || !need(k) || !need(v) || !need(a) || !need(beta) || !need(o))
     return fail(PACE_ERR_INVALID_ARG, "decode_step: a tensor pointer is NULL");
+  if (!io_aligned(q, k, v, a, beta, o))
+    return fail(PACE_ERR_INVALID_ARG, "decode_step: q, k, v, o must be 16-byte aligned, a and beta 4-byte aligned");
   PaceIO io{q, k, v, a, beta, o, 1};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -283,6 +291,8 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
   if (n_tokens == 0) return ok();
   if (!need(q) || !need(k) || !need(v) || !need(a) || !need(beta) || !need(o))
     return fail(PACE_ERR_INVALID_ARG, "prefill_chunk: a tensor pointer is NULL");
+  if (!io_aligned(q, k, v, a, beta, o))
+    return fail(PACE_ERR_INVALID_ARG, "prefill_chunk: q, k, v, o must be 16-byte aligned, a and beta 4-byte aligned");
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (state->cfg.state_mode != PACE_STATE_BF16) {

@@ -134,7 +134,8 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
  * q, k [B,H,d_k], v, o [B,H,d_v], a, beta [B,H]. In PACE_STATE_BF16 mode: no buffer, the bf16 state
  * is read, updated and written every token (the pages' per-token comparison point, [P1] 전제와 한계).
  * A unit whose buffer counter is outside 0..dP-1 (e.g. after importing a corrupted region) is left
- * unchanged and its output is zero. */
+ * unchanged and its output is zero. q, k, v and o must be 16-byte aligned, a and beta 4-byte aligned
+ * (PACE_ERR_INVALID_ARG otherwise, before any launch); the same holds for pace_prefill_chunk. */
 pace_status pace_decode_step(pace_state *state, const void *q, const void *k, const void *v, const float *a,
                              const float *beta, void *o, void *stream);
 

@@ -113,6 +113,31 @@ def test_empty_prefill_and_idle_flush_are_no_ops(P):
     assert torch.equal(before, run.state.region())
 
 
+def test_misaligned_io_is_rejected_before_any_launch(P):
+    """q, k, v, o are read and written as 8/16-byte vectors: an unaligned pointer is an argument error, raised on
+    the host; the state is untouched."""
+    import torch
+    wl = synth.workload("tiny")
+    run = PairRun(wl)
+    run.prefill(32)
+    torch.cuda.synchronize()
+    before = run.state.region().clone()
+    B, H, D = wl.B, wl.H, wl.d_k
+    buf = torch.zeros(B * H * D + 16, dtype=torch.bfloat16, device="cuda")
+    a = torch.full((B, H), 0.9, device="cuda")
+    ok = buf.data_ptr()
+    for bad in ("q", "o"):
+        ptrs = dict(q=ok, k=ok, v=ok, o=ok)
+        ptrs[bad] = ok + 2                              # bf16-aligned, not vector-aligned
+        with pytest.raises(P.PaceError) as ei:
+            P.pace_decode_step(run.state.handle, ptrs["q"], ptrs["k"], ptrs["v"], a, a, ptrs["o"], None)
+        assert ei.value.status == 1 and "aligned" in str(ei.value)
+        with pytest.raises(P.PaceError):
+            P.pace_prefill_chunk(run.state.handle, 1, ptrs["q"], ptrs["k"], ptrs["v"], a, a, ptrs["o"], None)
+    torch.cuda.synchronize()
+    assert torch.equal(before, run.state.region())
+
+
 def test_pending_buffer_flush_and_prefill_after_decode(P):
     wl = synth.workload("tiny")
     run = PairRun(wl)
