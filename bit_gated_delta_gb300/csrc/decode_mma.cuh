@@ -389,9 +389,9 @@ __device__ __forceinline__ void dm_load_token(const PaceDev &st, const PaceIO &i
 // their rows, packed int4 keys of the mixed buffer into a scratch area first) and the new one (written into
 // buffer slot m0). Leaves in shared memory the key rows (then the q digits), the values, a_t, the key
 // scales and the digit weights (vsc), G_t and G_m/G_t. Returns beta_t and the value scale of token t = lane.
-template <int D, int G, int MX>
+template <int D, int G, int MX, class AfterToken>
 __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, const TokenIn<D / 32> &tin,
-                         const MmaShared &sh, float &bt, float &sv_out) {
+                         const MmaShared &sh, float &bt, float &sv_out, AfterToken &&after_token) {
   constexpr int CPL = D / 32;
   const int lane = threadIdx.x & 31;
   const int col0 = CPL * lane;
@@ -480,6 +480,7 @@ __device__ void dm_stage(const PaceDev &st, int unit, int m0, int has_token, con
       sh.vsc[mt + 2] = sigma;
     }
   }
+  after_token();
   // the buffered rows have landed (the new token's rows above are other slots)
   cp_async_wait_all();
   __syncwarp();
@@ -1005,9 +1006,9 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
 
   // The loads go out in the order the step needs them: the buffer count (it gates the buffered rows) and the
-  // new token; once the count is known, the buffered rows, then the scales and zero points and the first
-  // column block's words; only then the L2 prefetch of the other blocks, so that the bulk of the state does
-  // not queue ahead of the staging loads.
+  // new token; once the count is known, the buffered rows, then the scales and zero points; the first column
+  // block's words once the new token has arrived; the L2 prefetch of the other blocks only after the tables.
+  // All units start together, so whatever is requested early delays the loads the staging waits for.
   const int m0 = (int)ldg_u32(st.m + unit);
   TokenIn<D / 32> tin;
   dm_load_token<D>(st, io, unit, has_token, tin);
@@ -1023,16 +1024,19 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   }
   dm_issue_scales<D, G, ZP>(st, unit, sh);
   uint32_t cw[PL][2][NPP][4];
-  dm_load_block<D, PL>(codes, 0, lane, cw);
-  constexpr uint32_t BLK = 2 * NPP * 128;        // words of one 32-column block in a plane
-  if (lane < PL) prefetch_l2(codes + lane * PLANE + BLK, (PLANE - BLK) * 4);
+
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
   const int nv = mt + (has_token ? 3 : 0);
   const int dpp = dm_dpp(dP);
   float bt, sv;
-  dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh, bt, sv);
+  // the first column block's words once the new token is in (they are first needed by the dots)
+  dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh, bt, sv, [&]() { dm_load_block<D, PL>(codes, 0, lane, cw); });
   dm_tables<D, G>(sh, nv, mt, dP, dpp, has_token, do_flush, bt, sv);
+  {                                              // the other blocks into L2, ahead of their loads
+    constexpr uint32_t BLK = 2 * NPP * 128;      // words of one 32-column block in a plane
+    if (lane < PL) prefetch_l2(codes + lane * PLANE + BLK, (PLANE - BLK) * 4);
+  }
 
 #pragma unroll 1
   for (int cb = 0; cb < D / 32; ++cb) {
