@@ -364,6 +364,7 @@ __device__ void bf16_column(const PaceDev &st, const PaceIO &io, long unit, int 
 template <int D>
 __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_enter();
   const long unit = blockIdx.x;
   const DecodeSmem L = decode_smem(D, st.dP, 0);
   const DecodeShared sh = decode_shared(smem, L);
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, con
 template <int D>
 __global__ void __launch_bounds__(D) decode_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_enter();
   const long unit = blockIdx.x;
   const DecodeSmem L = decode_smem(D, st.dP, 1);
   const DecodeShared sh = decode_shared(smem, L);
@@ -437,8 +439,9 @@ static cudaError_t launch_decode_t(const PaceDev &d, const PaceIO &io, int has_t
   }
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
-  kern<<<units, D, smem, s>>>(d, io, has_token);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(units), dim3(D), smem, s, attr);
+  return cudaLaunchKernelEx(&cfg, kern, d, io, has_token);
 }
 
 template <int D>
@@ -454,8 +457,9 @@ static cudaError_t launch_bf16buf_t(const PaceDev &d, const PaceIO &io, int has_
   }
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
-  kern<<<units, D, smem, s>>>(d, io, has_token);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(units), dim3(D), smem, s, attr);
+  return cudaLaunchKernelEx(&cfg, kern, d, io, has_token);
 }
 
 }  // namespace pace

@@ -15,6 +15,7 @@ __global__ void __launch_bounds__(2 * D) decode_bf16_kernel(const PaceDev st, co
   constexpr int RB = D / 4;           // rows per row block
   __shared__ float ks[D], qs[D], vs[D], us[D];
   __shared__ float part[4][D];
+  pdl_enter();
   const long unit = blockIdx.x;
   const int tid = threadIdx.x;
   const int cp = tid % NCP, rb = tid / NCP;
@@ -70,9 +71,8 @@ cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStre
   using namespace pace;
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
-  if (d.D == 128)
-    decode_bf16_kernel<128><<<units, 256, 0, s>>>(d, io);
-  else
-    decode_bf16_kernel<64><<<units, 128, 0, s>>>(d, io);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(units), dim3(2 * d.D), 0, s, attr);
+  return d.D == 128 ? cudaLaunchKernelEx(&cfg, decode_bf16_kernel<128>, d, io)
+                    : cudaLaunchKernelEx(&cfg, decode_bf16_kernel<64>, d, io);
 }

@@ -1053,6 +1053,7 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 template <int D, int G, int BITS, int ZP, int MX>
 __global__ void __launch_bounds__(DM_UPB * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : 12) / DM_UPB) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_enter();
   const int warp = threadIdx.x >> 5;
   const int HP = BITS == 4 ? st.H4 : st.H8;
   const int w = blockIdx.x * DM_UPB + warp;
@@ -1351,6 +1352,7 @@ __device__ void dc_tables(const MmaShared &sh, int nv, int mt, int dP, int has_t
 template <int D, int G, int BITS, int ZP, int MX>
 __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_enter();
   constexpr int NG = D / G, NPP = D / 64, PL = BITS / 4, NB = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int HP = BITS == 4 ? st.H4 : st.H8;
@@ -1424,14 +1426,15 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
   const long units = (long)d.B * (BITS == 4 ? d.H4 : d.H8);
   if (units == 0) return cudaSuccess;
   // one warp per unit while every SM holds 16 units' warps or more; below that, a CTA per unit
+  cudaLaunchAttribute attr[1];
   if (PACE_DM_CTA_PER_UNIT || units * DM_WARPS <= (long)dm_sm_count() * 16) {
-    decode_split_kernel<D, G, BITS, ZP, MX><<<(unsigned)units, DM_WARPS * 32, smem, s>>>(d, io, has_token);
-  } else {
-    // small blocks, so that the units spread evenly over the SMs (the slowest SM sets the step time)
-    const long blocks = (units + DM_UPB - 1) / DM_UPB;
-    decode_mma_kernel<D, G, BITS, ZP, MX><<<(unsigned)blocks, DM_UPB * 32, (size_t)DM_UPB * unit_smem, s>>>(d, io, has_token);
+    const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(DM_WARPS * 32), smem, s, attr);
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, BITS, ZP, MX>, d, io, has_token);
   }
-  return cudaGetLastError();
+  // small blocks, so that the units spread evenly over the SMs (the slowest SM sets the step time)
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((units + DM_UPB - 1) / DM_UPB)), dim3(DM_UPB * 32),
+                                            (size_t)DM_UPB * unit_smem, s, attr);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G, BITS, ZP, MX>, d, io, has_token);
 }
 
 template <int D, int G, int ZP, int MX>

@@ -17,6 +17,28 @@ __host__ __device__ inline size_t carve(size_t &off, size_t bytes, size_t align 
   return o;
 }
 
+// Programmatic dependent launch of the decode kernels: the next kernel of the stream may be scheduled as soon
+// as every block of this one has started (its blocks take SMs as ours leave), and a kernel touches no global
+// memory before every kernel it depends on has completed with its writes visible. Without the launch
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Launch configuration with the programmatic-serialization attribute (attr must outlive the launch call).
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute *attr) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
 __device__ __forceinline__ float load_io(const void *p, long idx, int io) {
