@@ -36,14 +36,13 @@ constexpr int DM_WARPS = 4;   // units (warps) per block
 #ifndef PACE_DM_CTA_PER_UNIT
 #define PACE_DM_CTA_PER_UNIT 0  // 1: the CTA-per-unit kernel at every batch size
 #endif
-#ifndef PACE_DM_UNITS_PER_BLOCK
-#define PACE_DM_UNITS_PER_BLOCK 1  // warps (units) per block of the warp-per-unit kernel
+#ifndef PACE_DM_WARPS_PER_UNIT
+#define PACE_DM_WARPS_PER_UNIT 0   // warps per unit of the warp-level kernel: 1, 2, or 0 = by batch size
 #endif
 #ifndef PACE_DM_MIN_WARPS
 #define PACE_DM_MIN_WARPS 16  // resident warps per SM the int4 kernels are compiled for (register cap)
 #endif
-constexpr int DM_UPB = PACE_DM_UNITS_PER_BLOCK;
-static_assert(PACE_DM_MIN_WARPS % DM_UPB == 0 && 12 % DM_UPB == 0, "units per block must divide the warps per SM");
+static_assert(PACE_DM_MIN_WARPS % 2 == 0, "the warp-level kernel is compiled for blocks of one and two warps");
 constexpr int PB_STRIDE = 40; // floats per row of the per-block dot table (conflict-free fragment stores)
 constexpr int UB_STRIDE = 36; // floats per row of the per-block replay table (conflict-free fragment loads)
 
@@ -992,9 +991,11 @@ __device__ __forceinline__ void dm_block(const PaceDev &st, const PaceIO &io, in
             make_uint4(cw[pl][m][pp][0], cw[pl][m][pp][1], cw[pl][m][pp][2], cw[pl][m][pp][3]);
 }
 
-template <int D, int G, int BITS, int ZP, int MX>
+template <int D, int G, int BITS, int ZP, int MX, int WU>
 __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
-                        const MmaShared &sh) {
+                        const MmaShared &sh, int part) {
+  // WU warps per unit: warp `part` runs the column blocks [cb0, cb1)
+  const int cb0 = WU == 1 ? 0 : part * (D / 32) / WU, cb1 = WU == 1 ? D / 32 : (part + 1) * (D / 32) / WU;
   constexpr int NG = D / G, NPP = D / 64, PL = BITS / 4;
   constexpr uint32_t PLANE = D * D / 8; // words per nibble plane
   const int lane = threadIdx.x & 31;
@@ -1031,38 +1032,39 @@ __device__ void dm_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   const int dpp = dm_dpp(dP);
   float bt, sv;
   // the first column block's words once the new token is in (they are first needed by the dots)
-  dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh, bt, sv, [&]() { dm_load_block<D, PL>(codes, 0, lane, cw); });
+  dm_stage<D, G, MX>(st, unit, m0, has_token, tin, sh, bt, sv, [&]() { dm_load_block<D, PL>(codes, cb0, lane, cw); });
   dm_tables<D, G>(sh, nv, mt, dP, dpp, has_token, do_flush, bt, sv);
-  {                                              // the other blocks into L2, ahead of their loads
+  if (cb1 - cb0 > 1) {                           // the warp's other blocks into L2, ahead of their loads
     constexpr uint32_t BLK = 2 * NPP * 128;      // words of one 32-column block in a plane
-    if (lane < PL) prefetch_l2(codes + lane * PLANE + BLK, (PLANE - BLK) * 4);
+    if (lane < PL) prefetch_l2(codes + lane * PLANE + (cb0 + 1) * BLK, (cb1 - cb0 - 1) * BLK * 4);
   }
 
 #pragma unroll 1
-  for (int cb = 0; cb < D / 32; ++cb) {
-    if (cb > 0 && do_flush) dm_load_block<D, PL>(codes, cb, lane, cw);
-    dm_block<D, G, BITS, ZP, MX>(st, io, unit, cb, m0, has_token, codes, scale, zpt, sh, cw, true);
+  for (int cb = cb0; cb < cb1; ++cb) {
+    if (cb > cb0 && do_flush) dm_load_block<D, PL>(codes, cb, lane, cw);
+    dm_block<D, G, BITS, ZP, MX>(st, io, unit, cb, m0, has_token, codes, scale, zpt, sh, cw, cb + 1 < cb1);
   }
-  __syncwarp();
-  if (lane == 0) st.m[unit] = do_flush ? 0 : mt;
+  // every warp of the unit has read the count before it moves on
+  if (WU > 1) __syncthreads(); else __syncwarp();
+  if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
 }
 
 // One launch per code pool (int4 heads, int8 heads), so that each path gets its own register allocation
 // (int4: 16 warps per SM at <= 128 registers; int8, with twice the code words live: 12 warps per SM).
 // Warp w of the launch handles pool unit w: sequence w / HP, the pool's head slot w % HP.
-template <int D, int G, int BITS, int ZP, int MX>
-__global__ void __launch_bounds__(DM_UPB * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : 12) / DM_UPB) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+template <int D, int G, int BITS, int ZP, int MX, int WU>
+__global__ void __launch_bounds__(WU * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : 12) / WU) decode_mma_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_enter();
   const int warp = threadIdx.x >> 5;
   const int HP = BITS == 4 ? st.H4 : st.H8;
-  const int w = blockIdx.x * DM_UPB + warp;
-  if (w >= st.B * HP) return;
+  const int w = blockIdx.x;                      // one unit per block, W warps per unit
+  if (w >= st.B * HP) return;                    // (the whole block)
   const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
   const MmaSmem L = mma_smem(D, G, st.dP, MX, ZP);
   const MmaShared sh = mma_shared(smem + (size_t)warp * L.total, L, st.dP);
-  dm_unit<D, G, BITS, ZP, MX>(st, io, b, h, b * st.H + h, has_token, sh);
+  dm_unit<D, G, BITS, ZP, MX, WU>(st, io, b, h, b * st.H + h, has_token, sh, warp);
 }
 
 // ---- cooperative form: the four warps of a CTA stage one unit together ---------------------------------------
@@ -1417,7 +1419,9 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
   static size_t opted = 0;
   const size_t smem = (size_t)DM_WARPS * unit_smem;   // the larger of the two launch shapes
   if (smem > 48 * 1024 && smem > opted) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_split_kernel<D, G, BITS, ZP, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
@@ -1427,14 +1431,18 @@ static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token
   if (units == 0) return cudaSuccess;
   // one warp per unit while every SM holds 16 units' warps or more; below that, a CTA per unit
   cudaLaunchAttribute attr[1];
-  if (PACE_DM_CTA_PER_UNIT || units * DM_WARPS <= (long)dm_sm_count() * 16) {
+  const long slots = (long)dm_sm_count() * 16;   // resident warps of the warp-level kernel
+  if (PACE_DM_CTA_PER_UNIT || (PACE_DM_WARPS_PER_UNIT == 0 && units * DM_WARPS <= slots)) {
     const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(DM_WARPS * 32), smem, s, attr);
     return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, BITS, ZP, MX>, d, io, has_token);
   }
-  // small blocks, so that the units spread evenly over the SMs (the slowest SM sets the step time)
-  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((units + DM_UPB - 1) / DM_UPB)), dim3(DM_UPB * 32),
-                                            (size_t)DM_UPB * unit_smem, s, attr);
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G, BITS, ZP, MX>, d, io, has_token);
+  // One unit per block. Each unit's warps stage it on their own and split its column blocks: while the units
+  // fill fewer than half the warp slots, two warps per unit halve the per-unit chain; otherwise one warp, and
+  // one-warp blocks spread the units evenly over the SMs (the slowest SM sets the step time).
+  const int W = PACE_DM_WARPS_PER_UNIT ? PACE_DM_WARPS_PER_UNIT : (units * 2 <= slots ? 2 : 1);
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(W * 32), (size_t)W * unit_smem, s, attr);
+  return W == 2 ? cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G, BITS, ZP, MX, 2>, d, io, has_token)
+                : cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G, BITS, ZP, MX, 1>, d, io, has_token);
 }
 
 template <int D, int G, int ZP, int MX>

@@ -43,6 +43,23 @@ def test_pace4_batch64_full_schedule(P):
     assert (read_blob(run.state).m() == 0).all()
 
 
+def test_pace4_two_warps_per_unit(P):
+    """Batch 24 x 32 heads = 768 units fill fewer than half the warp slots, so two warps share each unit (each
+    stages it and takes two of its four column blocks); outputs within the bar, codes of every rounding agree."""
+    wl = synth.workload("pace4", B=24)
+    run = PairRun(wl, sample=[(0, 0), (23, 31), (11, 17), (5, 2), (18, 30)], out_f32=True)
+    g, r = run.prefill(256)
+    assert rel_l2(g, r) <= 1e-3
+    run.check_round_and_sync()
+    for step in range(2 * wl.dP):
+        g, r = run.decode()
+        assert rel_l2(g, r) <= 1e-3, step
+        if (step + 1) % wl.dP == 0:
+            frac, dmax = run.check_round_and_sync()
+            assert frac >= 0.999 and dmax <= 1, (step, frac, dmax)
+    assert (read_blob(run.state).m() == 0).all()
+
+
 def test_pace4_free_running_drift(P):
     """Without re-synchronisation the two trajectories may take different roundings at near-ties (one
     code step apart); the outputs then drift apart slowly but stay close."""
