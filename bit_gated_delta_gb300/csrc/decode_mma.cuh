@@ -632,11 +632,25 @@ __device__ void dm_tables(const MmaShared &sh, int nv, int mt, int dP, int dpp, 
   }
   if (do_flush) {
     const int half = dpp >> 1;
-    for (int idx = lane; idx < D * half; idx += 32) {
-      const int i = idx / half, s = 2 * (idx - i * half);
-      const float k0 = s < mt ? (float)sh.krow[s * D + i] : 0.0f;
-      const float k1 = s + 1 < mt ? (float)sh.krow[(s + 1) * D + i] : 0.0f;
-      sh.kbf[idx] = bf16x2_bits(k0, k1);
+    if (half == 4) {                             // dP <= 8: lane = (token pair p, key quads), 4-byte row loads
+      const int p = lane & 3, s = 2 * p;
+      const bool z0 = s >= mt, z1 = s + 1 >= mt;
+#pragma unroll
+      for (int it = 0; it < D / 32; ++it) {
+        const int i0 = 4 * ((lane >> 2) + 8 * it);   // keys i0 .. i0 + 3
+        const uint32_t r0 = z0 ? 0u : *reinterpret_cast<const uint32_t *>(sh.krow + s * D + i0);
+        const uint32_t r1 = z1 ? 0u : *reinterpret_cast<const uint32_t *>(sh.krow + (s + 1) * D + i0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sh.kbf[(i0 + e) * 4 + p] = bf16x2_bits((float)(int8_t)(r0 >> (8 * e)), (float)(int8_t)(r1 >> (8 * e)));
+      }
+    } else {
+      for (int idx = lane; idx < D * half; idx += 32) {
+        const int i = idx / half, s = 2 * (idx - i * half);
+        const float k0 = s < mt ? (float)sh.krow[s * D + i] : 0.0f;
+        const float k1 = s + 1 < mt ? (float)sh.krow[(s + 1) * D + i] : 0.0f;
+        sh.kbf[idx] = bf16x2_bits(k0, k1);
+      }
     }
   }
   __syncwarp();
@@ -1378,12 +1392,12 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split
   __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
   uint8_t *zpt = zpm ? st.zp + (size_t)unit * NG * D : nullptr;
   const bool active = warp < NB;
+  const int m0 = (int)ldg_u32(st.m + unit);      // first: every warp's first wait is on the count
   uint32_t cw[PL][2][NPP][4];
   if (active) dm_load_block<D, PL>(codes, warp, lane, cw);
   float x[D / 32], xq[D / 32], an, bn;
   float4 bs;
   dc_issue<D, G, ZP, MX>(st, io, unit, has_token, sh0, warp, x, xq, bs, an, bn);
-  const int m0 = st.m[unit];
   if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
     cp_async_wait_all();                         // nothing may land in shared memory after the CTA leaves
     if (warp == 0 && has_token && m0 != 0)       // corrupted counter: leave the unit, emit zeros
