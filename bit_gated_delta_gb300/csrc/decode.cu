@@ -17,12 +17,14 @@ namespace pace {
 
 constexpr int VCHUNK = 8;   // dot-product vectors handled per pass over the codes
 
-// Vectors of the dot products (the buffered keys and q), padded to a multiple of 4.
-__host__ __device__ inline int dec_nvp(int dP) { return 4 * ((dP + 1 + 3) / 4); }
 
 struct DecodeSmem {
-  size_t kq, keyf, vf, P, U, kf, csum, vscale, a, beta, gam, Dm, W, cq, ck, red, qf, keyT, Ss, total;
+  size_t kq, keyf, vf, P, U, kf, csum, vscale, a, beta, gam, Dm, W, cq, ck, red, qf, ah, Ss, total;
 };
+
+// Rows of the tensor-core dot products of the buffered bf16 state: the mt key codes, then q as three bf16
+// parts, padded to whole 16-row tiles.
+__host__ __device__ inline int dec_arows(int dP) { return 16 * ((dP + 3 + 15) / 16); }
 
 __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
   DecodeSmem L;
@@ -30,7 +32,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
   L.kq = carve(off, (size_t)(dP + 2) * D);                     // int8 key codes (+ q halves)
   L.keyf = carve(off, fp32mode ? (size_t)(dP + 1) * D * 4 : 0); // fp32 keys (+ q), fp32 mode
   L.vf = carve(off, (size_t)dP * D * 4);                       // dequantized values
-  L.P = carve(off, (size_t)(dP + 2) * D * 4);                  // S_hat^T k_tau, S_hat^T q
+  L.P = carve(off, (size_t)(dP + 3) * D * 4);                  // S^T k_tau, S^T q (bf16 state: 3 q parts)
   L.U = carve(off, (size_t)dP * D * 4);                        // u_tau per column
   L.kf = carve(off, (size_t)dP * D * 4);                       // flush coefficients x keys
   L.csum = carve(off, (size_t)(dP + 2) * 4 * 4);               // per vector, per group code sums
@@ -44,8 +46,8 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
   L.ck = carve(off, (size_t)dP * 4);
   L.red = carve(off, 32 * 4);
   L.qf = carve(off, (size_t)D * 4);
-  L.keyT = carve(off, fp32mode ? 0 : (size_t)D * dec_nvp(dP) * 4);   // bf16 state: [i][vector] fp32 keys, q
-  L.Ss = carve(off, fp32mode ? 0 : (size_t)D * D * 2);                // bf16 state: the unit's state, staged
+  L.ah = carve(off, fp32mode ? 0 : (size_t)dec_arows(dP) * D * 2);   // bf16 state: bf16 rows (keys, q parts)
+  L.Ss = carve(off, fp32mode ? 0 : (size_t)D * D * 2, 128);           // bf16 state: the unit's state, staged
   L.total = carve(off, 0);
   return L;
 }
@@ -54,8 +56,8 @@ struct DecodeShared {
   int8_t *kq;
   float *keyf, *vf, *P, *U, *kf;
   int *csum;
-  float *vscale, *a, *beta, *gam, *Dm, *W, *cq, *ck, *red, *qf, *keyT;
-  __nv_bfloat16 *Ss;
+  float *vscale, *a, *beta, *gam, *Dm, *W, *cq, *ck, *red, *qf;
+  __nv_bfloat16 *ah, *Ss;
 };
 
 __device__ inline DecodeShared decode_shared(unsigned char *base, const DecodeSmem &L) {
@@ -77,7 +79,7 @@ __device__ inline DecodeShared decode_shared(unsigned char *base, const DecodeSm
   s.ck = reinterpret_cast<float *>(base + L.ck);
   s.red = reinterpret_cast<float *>(base + L.red);
   s.qf = reinterpret_cast<float *>(base + L.qf);
-  s.keyT = reinterpret_cast<float *>(base + L.keyT);
+  s.ah = reinterpret_cast<__nv_bfloat16 *>(base + L.ah);
   s.Ss = reinterpret_cast<__nv_bfloat16 *>(base + L.Ss);
   return s;
 }
@@ -243,7 +245,7 @@ __device__ void unit_tables(int mt, int has_token, int fp32mode, int dP, const D
 // Per-column replay of the buffered tokens (reduced form) and the readout o_j.
 template <int D>
 __device__ void recurrence(const PaceDev &st, const PaceIO &io, long unit, int nv, int mt, int has_token,
-                           int fp32mode, const DecodeShared &sh) {
+                           int qrows, const DecodeShared &sh) {
   const int j = threadIdx.x;
   const int dP = st.dP;
   for (int t = 0; t < mt; ++t) {
@@ -252,7 +254,7 @@ __device__ void recurrence(const PaceDev &st, const PaceIO &io, long unit, int n
     sh.U[t * D + j] = sh.beta[t] * acc;
   }
   if (has_token) {
-    const float R = fp32mode ? sh.P[mt * D + j] : sh.P[mt * D + j] + sh.P[(mt + 1) * D + j];
+    const float R = qrows == 1 ? sh.P[mt * D + j] : sh.P[mt * D + j] + (sh.P[(mt + 1) * D + j] + sh.P[(mt + 2) * D + j]);
     float o = sh.gam[mt - 1] * R;
     for (int s = 0; s < mt; ++s) o = fmaf(sh.cq[s], sh.U[s * D + j], o);
     store_io(io.o, unit * D + j, o, st.io);
@@ -300,62 +302,80 @@ __device__ void fp32_column(const PaceDev &st, const PaceIO &io, long unit, int 
   }
 }
 
-// Buffered bf16 state: the dot products with the unit's bf16 state, staged in shared memory at kernel entry
-// (each element feeds the key codes and q from the transposed table, four vectors per shared-memory load), the
-// replay, and at a rounding S_new = G_m S + sum_s (G_m/G_s) k_s u_s^T written back to global memory as bf16.
+// Element (i, j) of the staged bf16 state: rows of D values, 16-byte chunks XOR-swizzled by the row, so that
+// the eight rows of an ldmatrix tile fall in distinct banks.
+template <int D>
+__device__ __forceinline__ int ss_off(int i, int j) { return i * D + ((((j >> 3) ^ (i & 7)) << 3) | (j & 7)); }
+
+__device__ __forceinline__ void bb_ldsm_x4(uint32_t (&r)[4], const void *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"((uint32_t)__cvta_generic_to_shared(p)) : "memory");
+}
+__device__ __forceinline__ void bb_ldsm_x4_trans(uint32_t (&r)[4], const void *p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"((uint32_t)__cvta_generic_to_shared(p)) : "memory");
+}
+__device__ __forceinline__ void bb_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Buffered bf16 state: the dot products P[v][j] = sum_i A[v][i] S[i][j] on the tensor cores (bf16 MMA, fp32
+// accumulation) with A = the key codes of the mt buffered tokens (exact in bf16) and q as three bf16 parts
+// (q0 + q1 + q2 = q to 24 bits), B = the unit's state staged in shared memory (ldmatrix.trans); warp w takes
+// the 32 columns 32w.., one 16-row tile of A at a time. Then the replay and, at a rounding,
+// S_new = G_m S + sum_s (G_m/G_s) k_s u_s^T written back to global memory as bf16.
 template <int D>
 __device__ void bf16_column(const PaceDev &st, const PaceIO &io, long unit, int mt, int has_token, int do_flush,
                             const DecodeShared &sh) {
-  const int j = threadIdx.x;
-  const int nvp = dec_nvp(st.dP);
+  const int j = threadIdx.x, lane = j & 31, w = j >> 5;
+  const int g8 = lane >> 2, tq = lane & 3;
   __nv_bfloat16 *Sp = static_cast<__nv_bfloat16 *>(st.S) + unit * D * D;
   const __nv_bfloat16 *Ss = sh.Ss;
-  const int nv = mt + has_token;
-  for (int c0 = 0; c0 < nv; c0 += VCHUNK) {
-    float pf[VCHUNK];
+  const int nr = mt + (has_token ? 3 : 0);       // rows of A in use
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = lane >> 4;   // ldmatrix x4: A row, 8-key chunk
+  const int bkey = (lane & 7) + 8 * ((lane >> 3) & 1), bchk = lane >> 4;   // ldmatrix x4.trans: key, column chunk
+  for (int vt = 0; vt < (nr + 15) / 16; ++vt) {
+    float acc[4][4];
 #pragma unroll
-    for (int t = 0; t < VCHUNK; ++t) pf[t] = 0.0f;
-    if (nv - c0 <= 4) {                           // four vectors or fewer left: one table load per key
-#pragma unroll 8
-      for (int i = 0; i < D; ++i) {
-        const float s = __bfloat162float(Ss[i * D + j]);
-        const float4 k0 = *reinterpret_cast<const float4 *>(sh.keyT + i * nvp + c0);
-        pf[0] = fmaf(s, k0.x, pf[0]);
-        pf[1] = fmaf(s, k0.y, pf[1]);
-        pf[2] = fmaf(s, k0.z, pf[2]);
-        pf[3] = fmaf(s, k0.w, pf[3]);
-      }
-    } else {
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[n][e] = 0.0f;
 #pragma unroll 4
-      for (int i = 0; i < D; ++i) {
-        const float s = __bfloat162float(Ss[i * D + j]);
-        const float4 k0 = *reinterpret_cast<const float4 *>(sh.keyT + i * nvp + c0);
-        const float4 k1 = *reinterpret_cast<const float4 *>(sh.keyT + i * nvp + c0 + 4);
-        pf[0] = fmaf(s, k0.x, pf[0]);
-        pf[1] = fmaf(s, k0.y, pf[1]);
-        pf[2] = fmaf(s, k0.z, pf[2]);
-        pf[3] = fmaf(s, k0.w, pf[3]);
-        pf[4] = fmaf(s, k1.x, pf[4]);
-        pf[5] = fmaf(s, k1.y, pf[5]);
-        pf[6] = fmaf(s, k1.z, pf[6]);
-        pf[7] = fmaf(s, k1.w, pf[7]);
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[4];
+      bb_ldsm_x4(a, sh.ah + ss_off<D>(16 * vt + arow, 16 * ks + 8 * acol));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t b[4];
+        bb_ldsm_x4_trans(b, Ss + ss_off<D>(16 * ks + bkey, 32 * w + 16 * h + 8 * bchk));
+        bb_mma(acc[2 * h], a, b[0], b[1]);
+        bb_mma(acc[2 * h + 1], a, b[2], b[3]);
       }
     }
 #pragma unroll
-    for (int t = 0; t < VCHUNK; ++t) {
-      const int v = c0 + t;
-      if (v < mt) sh.P[v * D + j] = sh.vscale[v] * pf[t];    // key codes times the key scale
-      else if (v < nv) sh.P[v * D + j] = pf[t];               // q
+    for (int n = 0; n < 4; ++n) {
+      const int col = 32 * w + 8 * n + 2 * tq;
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int v = 16 * vt + g8 + 8 * hi;
+        if (v < nr) {
+          const float sc = v < mt ? sh.vscale[v] : 1.0f;   // key codes times the key scale; q parts as they are
+          *reinterpret_cast<float2 *>(sh.P + v * D + col) = make_float2(sc * acc[n][2 * hi], sc * acc[n][2 * hi + 1]);
+        }
+      }
     }
   }
-  recurrence<D>(st, io, unit, nv, mt, has_token, 1, sh);
+  __syncthreads();
+  recurrence<D>(st, io, unit, nr, mt, has_token, 3, sh);
   if (!do_flush) return;
   flush_coeffs<D>(mt, 0, sh);
   __syncthreads();
   const float gm = sh.gam[mt - 1];
   for (int i = 0; i < D; ++i) {
-    float x = gm * __bfloat162float(Ss[i * D + j]);
-    for (int s = 0; s < mt; ++s) x = fmaf(sh.kf[s * D + i], sh.U[s * D + j], x);
+    float x = gm * __bfloat162float(Ss[ss_off<D>(i, j)]);
+    for (int s2 = 0; s2 < mt; ++s2) x = fmaf(sh.kf[s2 * D + i], sh.U[s2 * D + j], x);
     Sp[i * D + j] = __float2bfloat16_rn(x);
   }
 }
@@ -372,9 +392,12 @@ __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, con
   {                                               // the unit's bf16 state, all copies in flight at once
     const char *src = reinterpret_cast<const char *>(static_cast<const __nv_bfloat16 *>(st.S) + unit * D * D);
     char *dst = reinterpret_cast<char *>(sh.Ss);
-    for (int c = j; c < D * D * 2 / 16; c += D)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst + 16 * c)),
+    for (int c = j; c < D * D * 2 / 16; c += D) {  // 16-byte chunk c = (row i, chunk cc), swizzled
+      const int i = c / (D / 8), cc = c - i * (D / 8);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                   ::"r"((uint32_t)__cvta_generic_to_shared(dst + 16 * (i * (D / 8) + (cc ^ (i & 7))))),
                    "l"(src + 16 * c) : "memory");
+    }
   }
   const int m0 = st.m[unit];
   if (m0 < 0 || m0 >= st.dP || (!has_token && m0 == 0)) {
@@ -388,10 +411,31 @@ __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, con
   if (has_token) append_token_i8<D>(st, io, unit, m0, sh);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  {                                               // keyT[i][v]: key codes of the mt tokens, then q, zero padded
-    const int nvp = dec_nvp(st.dP);
-    for (int v = 0; v < nvp; ++v)
-      sh.keyT[j * nvp + v] = v < mt ? (float)sh.kq[v * D + j] : (v == mt && has_token ? sh.qf[j] : 0.0f);
+  {                                               // bf16 rows of A: key codes, q in three parts, zeros
+    const int rows = dec_arows(st.dP);
+    for (int item = j; item < rows * (D / 8); item += D) {
+      const int v = item / (D / 8), k8 = 8 * (item - v * (D / 8));
+      uint32_t wv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x0 = 0.0f, x1 = 0.0f;
+        if (v < mt) {
+          x0 = (float)sh.kq[v * D + k8 + 2 * e];
+          x1 = (float)sh.kq[v * D + k8 + 2 * e + 1];
+        } else if (has_token && v < mt + 3) {
+          float q0 = sh.qf[k8 + 2 * e], q1 = sh.qf[k8 + 2 * e + 1];
+          for (int p = 0; p < v - mt; ++p) {           // the part's remainder: q - (earlier parts)
+            q0 -= bf16_round(q0);
+            q1 -= bf16_round(q1);
+          }
+          x0 = q0;
+          x1 = q1;
+        }
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(x0, x1);
+        wv[e] = *reinterpret_cast<const uint32_t *>(&pr);
+      }
+      *reinterpret_cast<uint4 *>(sh.ah + ss_off<D>(v, k8)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
   }
   unit_tables<D>(mt, has_token, 0, st.dP, sh);
   __syncthreads();
