@@ -135,34 +135,37 @@ __device__ void append_token(const PaceDev &st, const PaceIO &io, long unit, int
   sh.keyf[(m0 + 1) * D + j] = qx;            // q follows the keys
 }
 
-// Buffered bf16 state: stage buffered tokens 0..m0-1 (int8 key codes, dequantized values, scales).
+// Buffered bf16 state: the copies of buffered tokens 0..m0-1 in flight at once (int8 key codes straight into
+// their rows, value codes into a byte staging area), and their scalars (a, beta, key scale; the value scale
+// parked in cq until the values are converted).
 template <int D>
-__device__ void load_buffer_i8(const PaceDev &st, long unit, int m0, const DecodeShared &sh) {
-  const int j = threadIdx.x;
-  const int dP = st.dP;
-  const float *bs = st.buf_s + unit * dP * 4;
-  if (j < m0) {
-    sh.a[j] = bs[j * 4 + 0];
-    sh.beta[j] = bs[j * 4 + 1];
-    sh.vscale[j] = bs[j * 4 + 2];
+__device__ void issue_buffer_i8(const PaceDev &st, long unit, int m0, const DecodeShared &sh, int8_t *vstage) {
+  const int j = threadIdx.x, dP = st.dP;
+  const char *bk = static_cast<const char *>(st.buf_k) + unit * dP * D;
+  const char *bv = static_cast<const char *>(st.buf_v) + unit * dP * D;
+  for (int c = j; c < m0 * D / 16; c += D) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(sh.kq + 16 * c)),
+                 "l"(bk + 16 * c) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(vstage + 16 * c)),
+                 "l"(bv + 16 * c) : "memory");
   }
-  const int8_t *bk = static_cast<const int8_t *>(st.buf_k) + unit * dP * D;
-  const int8_t *bv = static_cast<const int8_t *>(st.buf_v) + unit * dP * D;
-  for (int t = 0; t < m0; ++t) {
-    sh.kq[t * D + j] = bk[t * D + j];
-    sh.vf[t * D + j] = bs[t * 4 + 3] * (float)bv[t * D + j];
+  if (j < m0) {
+    const float4 r = *reinterpret_cast<const float4 *>(st.buf_s + (unit * dP + j) * 4);
+    sh.a[j] = r.x;
+    sh.beta[j] = r.y;
+    sh.vscale[j] = r.z;
+    sh.cq[j] = r.w;
   }
 }
 
 // Buffered bf16 state: quantize the new token into slot m0 ([P1] 어떻게 동작하나: int8 keys and values, one
 // fp32 scale each), in shared and global memory, and stage q.
 template <int D>
-__device__ void append_token_i8(const PaceDev &st, const PaceIO &io, long unit, int m0, const DecodeShared &sh) {
+__device__ void append_token_i8(const PaceDev &st, const PaceIO &io, long unit, int m0, const DecodeShared &sh,
+                                float kx, float vx, float qx) {
   const int j = threadIdx.x;
   const int dP = st.dP;
-  const float kx = load_io(io.k, unit * D + j, st.io);
-  const float vx = load_io(io.v, unit * D + j, st.io);
-  sh.qf[j] = load_io(io.q, unit * D + j, st.io);
+  sh.qf[j] = qx;
   const float Ak = block_max(fabsf(kx), sh.red);
   const float Av = block_max(fabsf(vx), sh.red + 32 - D / 32);
   const int kc = buffer_code(kx, Ak, 127), vc = buffer_code(vx, Av, 127);
@@ -400,6 +403,12 @@ __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, con
     }
   }
   const int m0 = st.m[unit];
+  float kx = 0.0f, vx = 0.0f, qx = 0.0f;          // the new token, in flight with the count
+  if (has_token) {
+    kx = load_io(io.k, unit * D + j, st.io);
+    vx = load_io(io.v, unit * D + j, st.io);
+    qx = load_io(io.q, unit * D + j, st.io);
+  }
   if (m0 < 0 || m0 >= st.dP || (!has_token && m0 == 0)) {
     asm volatile("cp.async.wait_all;" ::: "memory");   // nothing may land in shared memory after the CTA leaves
     if (has_token && m0 != 0) store_io(io.o, unit * D + j, 0.0f, st.io);   // corrupted counter: emit zeros
@@ -407,10 +416,12 @@ __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, con
   }
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == st.dP;
-  load_buffer_i8<D>(st, unit, m0, sh);
-  if (has_token) append_token_i8<D>(st, io, unit, m0, sh);
+  int8_t *vstage = reinterpret_cast<int8_t *>(sh.kf);   // (the flush coefficients are written later)
+  issue_buffer_i8<D>(st, unit, m0, sh, vstage);
+  if (has_token) append_token_i8<D>(st, io, unit, m0, sh, kx, vx, qx);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
+  for (int t = 0; t < m0; ++t) sh.vf[t * D + j] = sh.cq[t] * (float)vstage[t * D + j];
   {                                               // bf16 rows of A: key codes, q in three parts, zeros
     const int rows = dec_arows(st.dP);
     for (int item = j; item < rows * (D / 8); item += D) {
