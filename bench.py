@@ -189,6 +189,11 @@ class DecodeSetup:
         self.R = R
         o = torch.empty(wl.B, wl.H, 256, wl.d_v, dtype=torch.bfloat16, device="cuda")
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # one untimed chunk on the last set first: the library's kernels are loaded on their first launch, a
+        # one-time host cost that would otherwise land inside the first timed chunk (the set is overwritten below)
+        x = synth.device_chunk_inputs(wl, 0, 256)
+        self.states[-1].prefill_chunk(x["q"], x["k"], x["v"], x["a"], x["beta"], o)
+        torch.cuda.synchronize()
         self.prefill_ms = 0.0
         for c, t0 in enumerate(range(0, prefill_tokens, 256)):
             x = synth.device_chunk_inputs(wl, t0, 256)
