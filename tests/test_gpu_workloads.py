@@ -60,6 +60,35 @@ def test_pace4_two_warps_per_unit(P):
     assert (read_blob(run.state).m() == 0).all()
 
 
+@pytest.mark.parametrize("B", [2, 24, 64])
+def test_steps_launched_back_to_back(P, B):
+    """A full period of decode steps on one state issued without a host synchronisation in between (each step's
+    kernel may be scheduled while the previous one drains and must wait for it before reading the state): the
+    outputs of every step and the codes of the rounding agree with the oracle. B=2: one CTA per unit; 24: two
+    warps per unit; 64: one warp per unit."""
+    import torch
+    wl = synth.workload("pace4", B=B)
+    sample = [(0, 0), (B - 1, 31), (B // 2, 17)]
+    run = PairRun(wl, sample=sample, out_f32=True)
+    run.prefill(256)
+    run.check_round_and_sync()
+    xs = [synth.token_inputs(wl, run.t + s, run.layer) for s in range(wl.dP)]
+    dev = [{k: run._dev(x[k], k in ("q", "k", "v")) for k in ("q", "k", "v", "a", "beta")} for x in xs]
+    outs = [torch.empty(wl.B, wl.H, wl.d_v, device="cuda") for _ in xs]
+    torch.cuda.synchronize()
+    for d, o in zip(dev, outs):
+        run.state.decode_step(d["q"], d["k"], d["v"], d["a"], d["beta"], o)
+    torch.cuda.synchronize()
+    for x, o in zip(xs, outs):
+        got = o.cpu().numpy()
+        for (b, h), u in run.units.items():
+            ref = O.decode_step(u, x["q"][b, h], x["k"][b, h], x["v"][b, h], x["a"][b, h], x["beta"][b, h])
+            assert rel_l2(got[b, h], ref) <= 1e-3
+    frac, dmax = run.codes_vs_oracle()
+    assert frac >= 0.999 and dmax <= 1, (frac, dmax)
+    assert (read_blob(run.state).m() == 0).all()
+
+
 def test_pace4_free_running_drift(P):
     """Without re-synchronisation the two trajectories may take different roundings at near-ties (one
     code step apart); the outputs then drift apart slowly but stay close."""
