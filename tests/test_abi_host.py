@@ -127,3 +127,28 @@ def test_resident_bits_formula_matches_oracle_accounting(P, zp, g, buf, n8, kh):
         full = P.pace_resident_bits(P.make_config(H, D, 16, dP=dP, group=g, zero_point=zp, buf_mode=buf), mask, False)
         kbytes = (0.5 if buf == 1 else 1.0) * D * dP * 16 * (H - kh)
         assert full - exact == pytest.approx(8.0 * kbytes / (16 * H * D * D), rel=1e-3, abs=1e-3)
+
+
+def test_bench_algorithmic_bytes_follow_the_state_layout(P):
+    """The roofline's numerator (bench.py) is the layout's bytes: per unit-step the packed int4 codes and bf16 group
+    scales read (and written at the rounding step), the buffered int8 entries read (k and v rows plus a, beta and
+    the two scales), the new entry written, q/k/v read and o written in bf16, a and beta, and the count. The state
+    and entry sizes are the ones pace_state_bytes allots per unit."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    H, D, B, dP, g = 32, 128, 64, 8, 64
+    state = D * D // 2 + (D // g) * D * 2                  # codes + scales of one unit
+    entry = 2 * D + 16                                     # int8 k and v rows + (a, beta, s_k, s_v)
+    n = P.pace_state_bytes(P.make_config(H, D, B, dP=dP, group=g))
+    assert B * H * (state + dP * entry + 4) <= n <= B * H * (state + dP * entry + 4) + 256 * 8
+    io = 3 * D * 2 + D * 2 + 8
+    for m0 in range(dP):
+        want = state + m0 * entry + entry + io + 8 + (state if m0 + 1 == dP else 0)
+        assert bench.decode_bytes_per_unit(D, g, dP, m0) == want
+    avg = bench.decode_bytes_period_avg(D, g, dP)
+    assert avg == 12056 and B * H * avg == 24690688
+    # per-token bf16: the bf16 state read and written every step, plus the token I/O
+    assert bench.bf16_bytes_per_unit(D) == 2 * D * D * 2 + io
+    # buffered bf16: the state read every step, written once per period, the same buffer traffic as PACE-4
+    assert bench.bf16buf_bytes_per_period_avg(D, dP) == D * D * 2 * (1 + 1 / dP) + sum(range(dP)) * entry / dP + entry + io + 8
