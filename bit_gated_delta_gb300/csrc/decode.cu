@@ -33,8 +33,10 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
   L.keyf = carve(off, fp32mode ? (size_t)(dP + 1) * D * 4 : 0); // fp32 keys (+ q), fp32 mode
   L.vf = carve(off, (size_t)dP * D * 4);                       // dequantized values
   L.P = carve(off, (size_t)(dP + 3) * D * 4);                  // S^T k_tau, S^T q (bf16 state: 3 q parts)
-  L.U = carve(off, (size_t)dP * D * 4);                        // u_tau per column
-  L.kf = carve(off, (size_t)dP * D * 4);                       // flush coefficients x keys
+  // u_tau per column; the bf16 state's bf16 rows (keys, q parts) share it, being done with before the replay
+  const size_t ub = (size_t)dP * D * 4, ab = (size_t)dec_arows(dP) * D * 2;
+  L.U = carve(off, fp32mode || ub >= ab ? ub : ab);
+  L.kf = carve(off, fp32mode ? (size_t)dP * D * 4 : 0);         // fp32 mode: flush coefficients x keys
   L.csum = carve(off, (size_t)(dP + 2) * 4 * 4);               // per vector, per group code sums
   L.vscale = carve(off, (size_t)(dP + 2) * 4);
   L.a = carve(off, (size_t)dP * 4);
@@ -46,7 +48,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int dP, int fp32mode) {
   L.ck = carve(off, (size_t)dP * 4);
   L.red = carve(off, 32 * 4);
   L.qf = carve(off, (size_t)D * 4);
-  L.ah = carve(off, fp32mode ? 0 : (size_t)dec_arows(dP) * D * 2);   // bf16 state: bf16 rows (keys, q parts)
+  L.ah = fp32mode ? carve(off, 0) : L.U;                       // bf16 state: bf16 rows (keys, q parts)
   L.Ss = carve(off, fp32mode ? 0 : (size_t)D * D * 2, 128);           // bf16 state: the unit's state, staged
   L.total = carve(off, 0);
   return L;
@@ -373,12 +375,10 @@ __device__ void bf16_column(const PaceDev &st, const PaceIO &io, long unit, int 
   __syncthreads();
   recurrence<D>(st, io, unit, nr, mt, has_token, 3, sh);
   if (!do_flush) return;
-  flush_coeffs<D>(mt, 0, sh);
-  __syncthreads();
   const float gm = sh.gam[mt - 1];
-  for (int i = 0; i < D; ++i) {
+  for (int i = 0; i < D; ++i) {                   // (G_m/G_s) s_ks k_s,i formed on the fly: one rounding, as stored
     float x = gm * __bfloat162float(Ss[ss_off<D>(i, j)]);
-    for (int s2 = 0; s2 < mt; ++s2) x = fmaf(sh.kf[s2 * D + i], sh.U[s2 * D + j], x);
+    for (int s2 = 0; s2 < mt; ++s2) x = fmaf(sh.ck[s2] * (float)sh.kq[s2 * D + i], sh.U[s2 * D + j], x);
     Sp[i * D + j] = __float2bfloat16_rn(x);
   }
 }
@@ -416,12 +416,13 @@ __global__ void __launch_bounds__(D) decode_bf16buf_kernel(const PaceDev st, con
   }
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == st.dP;
-  int8_t *vstage = reinterpret_cast<int8_t *>(sh.kf);   // (the flush coefficients are written later)
+  int8_t *vstage = reinterpret_cast<int8_t *>(sh.U);    // (the bf16 rows and the replay use it later)
   issue_buffer_i8<D>(st, unit, m0, sh, vstage);
   if (has_token) append_token_i8<D>(st, io, unit, m0, sh, kx, vx, qx);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   for (int t = 0; t < m0; ++t) sh.vf[t * D + j] = sh.cq[t] * (float)vstage[t * D + j];
+  __syncthreads();                                // the staged value codes are read before the rows overwrite them
   {                                               // bf16 rows of A: key codes, q in three parts, zeros
     const int rows = dec_arows(st.dP);
     for (int item = j; item < rows * (D / 8); item += D) {
