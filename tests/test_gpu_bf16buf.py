@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth
-from pace_testlib import PairRun, ensure_built, read_blob
+from pace_testlib import PairRun, check_bf16_state_and_sync, ensure_built, read_blob
 
 pytestmark = pytest.mark.gpu
 
@@ -27,13 +27,7 @@ def P():
 
 
 def check_state_and_sync(run, where):
-    got = run.gpu_state()
-    ref = np.stack([np.stack([run.units[(b, h)].S for h in range(run.wl.H)]) for b in range(run.wl.B)])
-    same = np.mean(got == ref.astype(np.float32))
-    floor = 2.0 ** -16 * np.abs(ref).max(axis=(2, 3), keepdims=True)
-    ulp = np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + floor
-    assert same >= 0.99 and ulp.all(), f"{where}: {same:.5f} identical, {np.mean(~ulp):.2e} beyond one ulp"
-    run.sync_state_from_gpu()
+    check_bf16_state_and_sync(run, where)
 
 
 @pytest.mark.parametrize("dP", [8, 1, 3, 32])

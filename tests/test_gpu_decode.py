@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import synth
-from pace_testlib import PairRun, ensure_built, read_blob, rel_l2
+from pace_testlib import PairRun, check_bf16_state_and_sync, ensure_built, read_blob, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -191,6 +191,21 @@ def test_bf16_per_token_comparison_kernel(P):
         g, r = run.decode()
         # bf16 rounding of the state every token: the trajectories may take different roundings
         assert rel_l2(g, r) <= 1e-2, f"step {step}"
+
+
+def test_bf16_per_token_state_every_step(P):
+    """The per-token bf16 comparison kernel rounds the state after every token: at every step its state is
+    within one bf16 ulp of the oracle's rounding of the same update (>= 99% identical), its outputs within one
+    ulp; then the oracle continues from the GPU's state."""
+    wl = synth.workload("pace4", B=2, H=4)
+    run = PairRun(wl, state_mode=P.PACE_STATE_BF16)
+    g, r = run.prefill(256)
+    check_out(run, g, r, "bf16-state prefill")
+    check_bf16_state_and_sync(run, "prefill")
+    for step in range(24):
+        g, r = run.decode()
+        check_out(run, g, r, f"step {step}")
+        check_bf16_state_and_sync(run, f"step {step}")
 
 
 @pytest.mark.parametrize("out_f32", [True, False])

@@ -43,6 +43,28 @@ def test_pace4_batch64_full_schedule(P):
     assert (read_blob(run.state).m() == 0).all()
 
 
+def test_pace4_batch64_bench_configuration(P):
+    """The configuration the benchmark times, end to end in bf16 I/O: two 256-token chunks through the
+    tensor-core prefill over all 2,048 units, then 256 decode steps with bf16 outputs (one warp per unit). The
+    sampled units meet the bars before any re-synchronisation: prefill outputs and every decode output within
+    one bf16 ulp (>= 99% equal to the bf16 rounding of the oracle's value), the levels, scales and zero points
+    of each chunk end and of every rounding."""
+    wl = synth.workload("pace4")
+    run = PairRun(wl, sample=SAMPLE64)
+    for c in range(wl.prefill // 256):
+        g, r = run.prefill(256)
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"chunk {c}: {msg}"
+        run.check_round_and_sync(f"chunk {c}")
+    for step in range(wl.decode):
+        g, r = run.decode()
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"step {step}: {msg}"
+        if (step + 1) % wl.dP == 0:
+            run.check_round_and_sync(f"step {step}")
+    assert (read_blob(run.state).m() == 0).all()
+
+
 def test_pace4_two_warps_per_unit(P):
     """Batch 24 x 32 heads = 768 units fill fewer than half the warp slots, so two warps share each unit (each
     stages it and takes two of its four column blocks); outputs within the bar, codes of every rounding agree."""
@@ -90,16 +112,25 @@ def test_steps_launched_back_to_back(P, B):
 
 
 def test_pace4_free_running_drift(P):
-    """Without re-synchronisation the two trajectories may take different roundings at near-ties (one
-    code step apart); the outputs then drift apart slowly but stay close."""
+    """Without re-synchronisation the two trajectories may take different roundings at near-ties (one code
+    step apart, R17); the outputs then drift apart slowly but stay close. The bar here is the drift bound 1e-2;
+    the 1e-3 bar applies per rounding period, from a common state (the other tests). What causes the drift is
+    counted: at every rounding the levels that differ from the oracle's are near-tie flips (one step), a
+    small fraction of the 64 x 16,384 sampled state values."""
     wl = synth.workload("pace4", B=8)
     run = PairRun(wl, sample=[(b, h) for b in range(8) for h in range(0, 32, 4)])
     for _ in range(2):
         run.prefill(256)
-    worst = 0.0
-    for _ in range(128):
+    worst, flips = 0.0, []
+    for step in range(128):
         g, r = run.decode()
         worst = max(worst, rel_l2(g, r))
+        if (step + 1) % wl.dP == 0:
+            frac, dmax = run.codes_vs_oracle()
+            flips.append(1.0 - frac)
+            assert dmax <= 2, (step, dmax)
+    print(f"free-running: worst output rel_l2 {worst:.3e}; level mismatch per rounding "
+          f"{min(flips):.2e} .. {max(flips):.2e}")
     assert worst <= 1e-2, worst
 
 
