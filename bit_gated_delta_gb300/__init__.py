@@ -10,7 +10,7 @@ import ctypes as C
 
 import numpy as np
 
-from ._lib import (PACE_BUF_FP32, PACE_BUF_INT8, PACE_BUF_MIXED, PACE_IO_BF16, PACE_IO_F32, PACE_MAX_DP,
+from ._lib import (PACE_BUF_FP32, PACE_BUF_INT8, PACE_BUF_MIXED, PACE_ERR_TIMEOUT, PACE_IO_BF16, PACE_IO_F32, PACE_MAX_DP,
                    PACE_MAX_HEADS, PACE_STATE_BF16, PACE_STATE_BF16_BUF, PACE_STATE_FP32, PACE_STATE_QUANT, PaceError, check, lib,
                    pace_config, pace_layout)
 
@@ -19,7 +19,8 @@ __all__ = [
     "pace_state_get_layout", "pace_prefill_chunk", "pace_decode_step", "pace_flush", "pace_assign_heads",
     "pace_quantize_state", "pace_dequantize_state", "pace_calib_error_energy", "pace_calib_error_energy_axis",
     "pace_state_export",
-    "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_last_error", "pace_version", "PaceState", "PaceError",
+    "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_test_wait_probe", "pace_last_error", "pace_version",
+    "PaceState", "PaceError", "PACE_ERR_TIMEOUT",
     "PACE_STATE_QUANT", "PACE_STATE_FP32", "PACE_STATE_BF16", "PACE_STATE_BF16_BUF", "PACE_BUF_INT8", "PACE_BUF_MIXED",
     "PACE_BUF_FP32", "PACE_IO_BF16", "PACE_IO_F32", "PACE_MAX_HEADS", "PACE_MAX_DP",
 ]
@@ -141,6 +142,12 @@ def pace_get_status(handle, clear: bool = False, stream=None) -> int:
     out = C.c_int()
     check(lib().pace_get_status(handle, int(clear), C.byref(out), _stream(stream)))
     return out.value
+
+
+def pace_test_wait_probe(handle, ns: int) -> None:
+    """Failure-detection hook: the state's tensor-core prefill launches first wait at most ns nanoseconds on a
+    barrier that nothing signals and report the timeout; 0 turns it off."""
+    check(lib().pace_test_wait_probe(handle, int(ns)))
 
 
 def pace_resident_bits(cfg: pace_config, head_is_int8=None, literal_formula: bool = True) -> float:

@@ -63,6 +63,7 @@ _SIGS = {
     "pace_state_import": (_I, [_VP, _VP, _SZ, _VP]),
     "pace_resident_bits": (_D, [C.POINTER(pace_config), _PU8, _I]),
     "pace_get_status": (_I, [_VP, _I, C.POINTER(C.c_int), _VP]),
+    "pace_test_wait_probe": (_I, [_VP, C.c_uint32]),
 }
 
 

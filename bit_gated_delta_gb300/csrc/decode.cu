@@ -486,13 +486,8 @@ template <int D>
 static cudaError_t launch_decode_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
   const size_t smem = decode_smem(D, d.dP, 1).total;
   auto kern = decode_kernel<D>;
-  static size_t opted = 48 * 1024;                // dynamic shared memory allowed so far
-  if (smem > opted) {
-    const size_t most = decode_smem(D, PACE_MAX_DP, 1).total;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
-    if (e != cudaSuccess) return e;
-    opted = most;
-  }
+  const cudaError_t e = smem_opt_in<decode_kernel<D>>(smem);
+  if (e != cudaSuccess) return e;
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
@@ -504,13 +499,8 @@ template <int D>
 static cudaError_t launch_bf16buf_t(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
   const size_t smem = decode_smem(D, d.dP, 0).total;
   auto kern = decode_bf16buf_kernel<D>;
-  static size_t opted = 48 * 1024;
-  if (smem > opted) {
-    const size_t most = decode_smem(D, PACE_MAX_DP, 0).total;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
-    if (e != cudaSuccess) return e;
-    opted = most;
-  }
+  const cudaError_t e = smem_opt_in<decode_bf16buf_kernel<D>>(smem);
+  if (e != cudaSuccess) return e;
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];

@@ -1,0 +1,817 @@
+// PACE decode step with fused flush, on the folded readout ([P1] 어떻게 동작하나: round once every dP tokens,
+// the buffered tokens applied together at the flush; [P2] 1. Key Terms & Definitions: the gated delta rule).
+//
+// Between two roundings the state of a unit is S_t = G_t S_hat + sum_{s<=t} (G_t/G_s) k_s u_s^T, G_t = a_1 .. a_t,
+// so replaying the m buffered tokens is one unit lower-triangular system per column j, shared by all columns:
+//   (I + L) u_j = diag(beta) r_j,   r_tj = v_tj - G_t (S_hat^T k_t)_j,   L_ts = beta_t (G_t/G_s) k_s.k_t  (s < t).
+// The output of the step does not need u. With cq_s = (G_m/G_s) k_s.q and c = diag(beta) (I + L)^-T cq,
+//   o = S_m^T q = G_m S_hat^T q + sum_s cq_s u_s = S_hat^T y + V^T c,   y = G_m q - sum_t c_t G_t k_t,
+// so a step without a rounding reads the packed state once against a single vector y. The per-unit work is an
+// 8 x 8 Gram matrix of the buffered int8 keys (one integer tensor-core MMA per 32 keys, exact), a back
+// substitution across lanes, and y; the state is then contracted with y's three int8 digits (a 24-bit fixed-point
+// image) on the tensor cores, straight from the packed nibbles:
+//   M = state columns (A: the lane's own packed words as fp16 1024 + u, or 1024 + 16u for the second 8 keys of a
+//   16-key step), N = the digit rows of y (B: fp16, second-half keys scaled by 1/16), K = keys.
+// Every product and partial sum is an exact integer in fp32; each key-axis group's accumulator starts at minus the
+// contribution of the zero level (computed by the same MMA from a constant operand), so the group fold is one
+// paired multiply-add by the group scale. The rounding step adds the buffered keys as a second N tile, replays
+// each column (four columns per lane) and requantizes the state per key-axis group as in decode_mma.cuh.
+#pragma once
+
+#include "decode_mma.cuh"
+
+namespace pace {
+
+constexpr int DF_TOK = 8;   // buffered tokens per unit this kernel handles (dP <= 8)
+
+struct FoldSmem {
+  size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, gram, qk, Lm, tk, ck, total;
+};
+// Per-warp work area. int8 rows use a stride of D + 16 bytes and fp16 digit rows D + 8 halves, so that the
+// fragment loads of the eight rows of a tile fall in distinct banks.
+__host__ __device__ inline FoldSmem fold_smem(int D, int G, int mixed, int zp) {
+  FoldSmem L;
+  size_t off = 0;
+  L.krow = carve(off, (size_t)11 * (D + 16));               // key codes of tokens 0..7, then the 3 digits of q
+  L.vrow = carve(off, (size_t)DF_TOK * D * (mixed ? 2 : 1)); // value codes (int8) or bf16 values
+  L.ydig = carve(off, (size_t)3 * (D + 8) * 2);              // fp16 digit rows of y
+  L.ssc = carve(off, (size_t)(D / G) * D * 2);               // group scales (bf16), as resident
+  L.szp = carve(off, zp ? (size_t)(D / G) * D : 0);          // zero points
+  L.po = carve(off, (size_t)D * 4);                          // S_hat^T y per column
+  L.pb = carve(off, (size_t)DF_TOK * D * 4);                 // rounding step: P_t then u_t [t][j]; packed
+                                                             // int4 keys of the mixed buffer while staging
+  L.kbf = carve(off, (size_t)D * 4 * 4);                     // flush B operand: bf16 pairs of int8 keys [i][pair]
+  L.gram = carve(off, 64 * 4);                               // k_s.k_t (integers)
+  L.qk = carve(off, 3 * 8 * 4);                              // (q digit d).k_t (integers)
+  L.Lm = carve(off, 64 * 4);                                 // L[t][s]
+  L.tk = carve(off, DF_TOK * 16);                            // per token: G_t s_kt, beta_t, s_vt, 0
+  L.ck = carve(off, DF_TOK * 4);                             // flush coefficient (G_m/G_s) s_ks
+  L.total = carve(off, 0, 16);
+  return L;
+}
+
+__device__ __forceinline__ void imma_s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lds32(const void *p) { return *reinterpret_cast<const uint32_t *>(p); }
+// Signed byte e of x as a float.
+__device__ __forceinline__ float sbyte(uint32_t x, int e) { return (float)(int)(int8_t)(x >> (8 * e)); }
+// N consecutive outputs from element idx (N = 1, 2 or 4; the output pointer is 16-byte aligned, idx a multiple of N).
+template <int N>
+__device__ __forceinline__ void store_io_vec(void *p, size_t idx, const float (&x)[N], int io) {
+  if (io == PACE_IO_F32) {
+    float *f = static_cast<float *>(p) + idx;
+    if constexpr (N == 4) *reinterpret_cast<float4 *>(f) = make_float4(x[0], x[1], x[2], x[3]);
+    else if constexpr (N == 2) *reinterpret_cast<float2 *>(f) = make_float2(x[0], x[1]);
+    else f[0] = x[0];
+  } else {
+    __nv_bfloat16 *h = static_cast<__nv_bfloat16 *>(p) + idx;
+    if constexpr (N == 4) *reinterpret_cast<uint2 *>(h) = make_uint2(bf16x2_bits(x[0], x[1]), bf16x2_bits(x[2], x[3]));
+    else if constexpr (N == 2) *reinterpret_cast<uint32_t *>(h) = bf16x2_bits(x[0], x[1]);
+    else h[0] = __float2bfloat16_rn(x[0]);
+  }
+}
+
+// The lane's packed words of M-tile mt (columns 16 mt .. 16 mt + 15), one 16-byte vector per 64 keys and plane.
+template <int D, int PL>
+__device__ __forceinline__ void df_load_tile(const uint32_t *codes, int mt, int lane, uint32_t (&cw)[PL][D / 64][4]) {
+  constexpr int NPP = D / 64;
+#pragma unroll
+  for (int pl = 0; pl < PL; ++pl)
+#pragma unroll
+    for (int pp = 0; pp < NPP; ++pp) {
+      const uint4 v = ldg_v4(codes + pl * (D * D / 8) + ((mt * NPP + pp) * 32 + lane) * 4);
+      cw[pl][pp][0] = v.x;
+      cw[pl][pp][1] = v.y;
+      cw[pl][pp][2] = v.z;
+      cw[pl][pp][3] = v.w;
+    }
+}
+
+// A fragment (M = columns 16mt + g8 and + 8, K = the 16 keys of step ks) from the lane's words of that M-tile.
+template <int D, int PL>
+__device__ __forceinline__ void df_afrag(const uint32_t (&cw)[PL][D / 64][4], int pl, int ks, uint32_t (&a)[4]) {
+  const int p = ks >> 1;
+  uint32_t w0 = cw[pl][p >> 1][p & 1], w1 = cw[pl][p >> 1][2 + (p & 1)];
+  if (ks & 1) {
+    w0 >>= 8;
+    w1 >>= 8;
+  }
+  a[0] = (w0 & 0x000F000Fu) | 0x64006400u;
+  a[1] = (w1 & 0x000F000Fu) | 0x64006400u;
+  a[2] = (w0 & 0x00F000F0u) | 0x64006400u;
+  a[3] = (w1 & 0x00F000F0u) | 0x64006400u;
+}
+// The A fragment of a constant word (every code of the tile equal).
+__device__ __forceinline__ void df_afrag_const(uint32_t w, uint32_t (&a)[4]) {
+  a[0] = a[1] = (w & 0x000F000Fu) | 0x64006400u;
+  a[2] = a[3] = (w & 0x00F000F0u) | 0x64006400u;
+}
+
+// Offsets of one group for the B operand b (the fragments of its G/16 key steps): the MMA of a constant code word.
+// off[e] = sum_i A_w[i] B[i][n] for the lane's two N columns n = 2tq, 2tq + 1 (every row of the tile is equal).
+template <int KSG>
+__device__ __forceinline__ void df_offset(uint32_t w, const uint32_t (*b)[2], float (&off)[2]) {
+  uint32_t a[4];
+  df_afrag_const(w, a);
+  float d[4];
+  mma_f16_z(d, a, b[0][0], b[0][1]);
+#pragma unroll
+  for (int kk = 1; kk < KSG; ++kk) mma_f16(d, a, b[kk][0], b[kk][1]);
+  off[0] = d[0];
+  off[1] = d[1];
+}
+// The pattern whose MMA is the plain sum of the B values of a group (second-half keys, stored / 16, count 16x).
+__device__ __forceinline__ void df_afrag_ones(uint32_t (&a)[4]) {
+  a[0] = a[1] = 0x3C003C00u;   // 1.0
+  a[2] = a[3] = 0x4C004C00u;   // 16.0
+}
+template <int KSG>
+__device__ __forceinline__ void df_sum(const uint32_t (*b)[2], float (&t2)[2]) {
+  uint32_t a[4];
+  df_afrag_ones(a);
+  float d[4];
+  mma_f16_z(d, a, b[0][0], b[0][1]);
+#pragma unroll
+  for (int kk = 1; kk < KSG; ++kk) mma_f16(d, a, b[kk][0], b[kk][1]);
+  t2[0] = d[0];
+  t2[1] = d[1];
+}
+
+// One unit: staging, tables, the folded readout and (at m = dP) the rounding. WU warps share the unit: each
+// stages it on its own and takes D/16/WU of its M-tiles.
+template <int D, int G, int BITS, int ZP, int MX, int WU>
+__device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
+                        unsigned char *wsm, int part) {
+  constexpr int CPL = D / 32, NG = D / G, MT = D / 16, NPP = D / 64, PL = BITS / 4, KS = D / 16, KSG = G / 16;
+  constexpr int RS = D + 16, YS = D + 8, MTW = MT / WU, CW = D / WU, CPW = CW / 32;
+  constexpr int OFF = 1 << (BITS - 1);
+  constexpr int NKG = G / 8;
+  static_assert(MTW >= 1 && CPW >= 1, "warps per unit");
+  const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
+  const int dP = st.dP;
+  const FoldSmem L = fold_smem(D, G, MX, ZP);
+  int8_t *krow = reinterpret_cast<int8_t *>(wsm + L.krow);
+  unsigned char *vrow = wsm + L.vrow;
+  __half *ydig = reinterpret_cast<__half *>(wsm + L.ydig);
+  __nv_bfloat16 *ssc = reinterpret_cast<__nv_bfloat16 *>(wsm + L.ssc);
+  uint8_t *szp = wsm + L.szp;
+  float *po = reinterpret_cast<float *>(wsm + L.po);
+  float *pb = reinterpret_cast<float *>(wsm + L.pb);
+  uint32_t *kbf = reinterpret_cast<uint32_t *>(wsm + L.kbf);
+  float *gram = reinterpret_cast<float *>(wsm + L.gram);
+  float *qk = reinterpret_cast<float *>(wsm + L.qk);
+  float *Lm = reinterpret_cast<float *>(wsm + L.Lm);
+  float4 *tk = reinterpret_cast<float4 *>(wsm + L.tk);
+  float *ckf = reinterpret_cast<float *>(wsm + L.ck);
+
+  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
+                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
+  __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
+  uint8_t *zpt = ZP ? st.zp + (size_t)unit * NG * D : nullptr;
+
+  // ---- loads, in the order the step needs them: the count and the new token; then the buffered rows, their
+  // scalars, the scales; the first code tiles once the new token is in
+  const int m0 = (int)ldg_u32(st.m + unit);
+  TokenIn<CPL> tin;
+  dm_load_token<D>(st, io, unit, has_token, tin);
+  if (m0 < 0 || m0 >= dP || (!has_token && m0 == 0)) {
+    if (part == 0 && has_token && m0 != 0)       // corrupted counter: leave the unit, emit zeros
+      for (int c = lane; c < D; c += 32) store_io(io.o, (long)unit * D + c, 0.0f, st.io);
+    return;                                      // (or a flush with nothing pending)
+  }
+  const int mt = m0 + has_token;
+  const int do_flush = !has_token || mt == dP;
+  const size_t ku = key_unit(st, unit);
+  float4 bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);   // lane t < mt: token t's a, beta, key scale, value scale
+  if (m0 > 0) {
+    constexpr int rk = MX ? D / 2 : D, rv = MX ? 2 * D : D;
+    const char *gk = static_cast<const char *>(st.buf_k) + ku * dP * rk;
+    const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
+    if (MX) {
+      unsigned char *scr = reinterpret_cast<unsigned char *>(pb);
+      for (int c = lane; c < m0 * rk / 16; c += 32) cp_async16(scr + 16 * c, gk + 16 * c);
+    } else {
+      for (int c = lane; c < m0 * (D / 16); c += 32) {
+        const int t = c / (D / 16), q = c - t * (D / 16);
+        cp_async16(krow + t * RS + 16 * q, gk + 16 * c);
+      }
+    }
+    for (int c = lane; c < m0 * rv / 16; c += 32) cp_async16(vrow + 16 * c, gv + 16 * c);
+    if (lane < m0) bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
+  }
+  {
+    const char *gs = reinterpret_cast<const char *>(scale);
+    for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(ssc) + 16 * c, gs + 16 * c);
+    if (ZP) {
+      const char *gz = reinterpret_cast<const char *>(zpt);
+      for (int c = lane; c < NG * D / 16; c += 32) cp_async16(szp + 16 * c, gz + 16 * c);
+    }
+  }
+
+  // ---- the new token: buffer slot m0 (global and shared), its scalars; q as three int8 digit rows
+  float sq = 0.0f;                                 // scale of the q digits
+  if (has_token) {
+    const int col0 = CPL * lane;
+    float mk = 0.0f, mv = 0.0f, mq = 0.0f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      mk = fmaxf(mk, fabsf(tin.kx[c]));
+      mv = fmaxf(mv, fabsf(tin.vx[c]));
+      mq = fmaxf(mq, fabsf(tin.qx[c]));
+    }
+    const float Ak = warp_max(mk), Av = warp_max(mv), Aq = warp_max(mq);
+    const int qkm = MX ? 7 : 127;
+    const bool kz = !(Ak >= FLT_MIN);
+    const float rkk = kz ? 0.0f : __fdiv_rn((float)qkm, Ak);
+    const float sk = kz ? 0.0f : __fdiv_rn(Ak, (float)qkm);
+    int ck[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) ck[c] = min(max(__float2int_rn(__fmul_rn(tin.kx[c], rkk)), -qkm), qkm);
+    dm_store_bytes<CPL>(krow + m0 * RS + col0, ck);
+    float sv = 0.0f;
+    const bool kw = part == 0 && key_writer(st, unit);
+    if (MX) {
+      uint8_t *bk = static_cast<uint8_t *>(st.buf_k) + (ku * dP + m0) * (D / 2) + col0 / 2;
+      if (kw) {
+#pragma unroll
+        for (int c = 0; c < CPL; c += 2) bk[c / 2] = (uint8_t)((ck[c] + 8) | ((ck[c + 1] + 8) << 4));
+      }
+      __nv_bfloat16 *bv = static_cast<__nv_bfloat16 *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0;
+      uint32_t *vr = reinterpret_cast<uint32_t *>(vrow + ((size_t)m0 * D + col0) * 2);
+#pragma unroll
+      for (int c = 0; c < CPL; c += 2) {
+        const __nv_bfloat162 pv = __floats2bfloat162_rn(tin.vx[c], tin.vx[c + 1]);
+        if (part == 0) *reinterpret_cast<__nv_bfloat162 *>(bv + c) = pv;
+        vr[c / 2] = *reinterpret_cast<const uint32_t *>(&pv);
+      }
+    } else {
+      const bool vz = !(Av >= FLT_MIN);
+      const float rvv = vz ? 0.0f : __fdiv_rn(127.0f, Av);
+      sv = vz ? 0.0f : __fdiv_rn(Av, 127.0f);
+      int cv[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) cv[c] = min(max(__float2int_rn(__fmul_rn(tin.vx[c], rvv)), -127), 127);
+      if (kw) dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + (ku * dP + m0) * D + col0, ck);
+      if (part == 0) dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0, cv);
+      dm_store_bytes<CPL>(vrow + m0 * D + col0, cv);
+    }
+    if (lane == m0) bs = make_float4(tin.an, tin.bn, sk, sv);
+    if (part == 0 && lane == 0)
+      *reinterpret_cast<float4 *>(st.buf_s + ((size_t)unit * dP + m0) * 4) = make_float4(tin.an, tin.bn, sk, sv);
+    // q ~= sq (65536 d2 + 256 d1 + d0), balanced base-256 digits in [-128, 127] (rows 8, 9, 10)
+    const float QMAX = 8323072.0f;
+    const bool qz = !(Aq >= FLT_MIN);
+    sq = qz ? 0.0f : __fdiv_rn(Aq, QMAX);
+    const float rq = qz ? 0.0f : __fdiv_rn(QMAX, Aq);
+    int d2[CPL], d1[CPL], d0[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      const int qi = min(max(__float2int_rn(tin.qx[c] * rq), -8323072), 8323072);
+      const int q1 = (qi + 128) >> 8;
+      d0[c] = qi - (q1 << 8);
+      d2[c] = (q1 + 128) >> 8;
+      d1[c] = q1 - (d2[c] << 8);
+    }
+    dm_store_bytes<CPL>(krow + 8 * RS + col0, d2);
+    dm_store_bytes<CPL>(krow + 9 * RS + col0, d1);
+    dm_store_bytes<CPL>(krow + 10 * RS + col0, d0);
+  }
+  // the first two code tiles of this warp, once the new token is in
+  const int mt0 = part * MTW;
+  uint32_t cwA[PL][NPP][4], cwB[PL][NPP][4];
+  df_load_tile<D, PL>(codes, mt0, lane, cwA);
+  if (MTW > 1) df_load_tile<D, PL>(codes, mt0 + 1, lane, cwB);
+  cp_async_wait_all();
+  __syncwarp();
+  if (MX) {                                        // packed int4 keys (code + 8) -> int8 rows
+    const unsigned char *scr = reinterpret_cast<const unsigned char *>(pb);
+    for (int t = 0; t < m0; ++t) {
+      if (lane < D / 8) {
+        const uint32_t nb = *reinterpret_cast<const uint32_t *>(scr + t * (D / 2) + 4 * lane);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          lo |= (uint32_t)(((int)((nb >> (8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
+          hi |= (uint32_t)(((int)((nb >> (16 + 8 * (e >> 1) + 4 * (e & 1))) & 0xF) - 8) & 0xFF) << (8 * e);
+        }
+        *reinterpret_cast<uint2 *>(krow + t * RS + 8 * lane) = make_uint2(lo, hi);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- Gram products k_s.k_t and (q digit).k_t: integer MMA, A = [keys 0..7 | q digits] (M), B = keys (N)
+  {
+    int gacc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int kb = 0; kb < D / 32; ++kb) {
+      const int off = 32 * kb + 4 * tq;
+      const uint32_t a0 = lds32(krow + g8 * RS + off), a2 = lds32(krow + g8 * RS + off + 16);
+      const uint32_t a1 = g8 < 3 ? lds32(krow + (8 + g8) * RS + off) : 0u;
+      const uint32_t a3 = g8 < 3 ? lds32(krow + (8 + g8) * RS + off + 16) : 0u;
+      imma_s8(gacc, a0, a1, a2, a3, a0, a2);
+    }
+    *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2((float)gacc[0], (float)gacc[1]);
+    if (g8 < 3) *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2((float)gacc[2], (float)gacc[3]);
+  }
+  __syncwarp();
+
+  // ---- per-token tables (lane s = token s): decay products, L's column s, the flush coefficient
+  const int s = lane;
+  const float a_s = bs.x, beta_s = bs.y, sk_s = bs.z, sv_s = bs.w;
+  float Gs = 1.0f, gmr = 1.0f;                     // G_s = a_1 .. a_s ; G_m / G_s
+  float Lc[DF_TOK];                                // L_ts = beta_t (G_t/G_s) s_ks s_kt (k_s.k_t), t > s
+  {
+    float grow[DF_TOK];
+    *reinterpret_cast<float4 *>(grow) = *reinterpret_cast<const float4 *>(gram + (s & 7) * 8);
+    *reinterpret_cast<float4 *>(grow + 4) = *reinterpret_cast<const float4 *>(gram + (s & 7) * 8 + 4);
+    const float bsk = beta_s * sk_s;
+    float p = 1.0f;                                // a_{s+1} .. a_t
+#pragma unroll
+    for (int t = 0; t < DF_TOK; ++t) {
+      const float at = __shfl_sync(0xffffffffu, a_s, t);
+      const float bt = __shfl_sync(0xffffffffu, bsk, t);
+      if (t <= s) Gs *= at;
+      if (t > s && t < mt) p *= at;
+      if (t == mt - 1) gmr = p;
+      Lc[t] = (t > s && t < mt) ? bt * p * sk_s * grow[t] : 0.0f;
+    }
+  }
+  const float Gm = __shfl_sync(0xffffffffu, Gs, mt - 1);
+  if (do_flush) {
+    if (s < mt) {
+      tk[s] = make_float4(Gs * sk_s, beta_s, MX ? 1.0f : sv_s, 0.0f);
+      ckf[s] = gmr * sk_s;
+#pragma unroll
+      for (int t = 0; t < DF_TOK; ++t) Lm[t * 8 + s] = Lc[t];
+    }
+    // the flush B operand: kbf[i][p] = bf16 pair (k_{2p,i}, k_{2p+1,i}), zero for tokens >= mt
+    {
+      const int p = lane & 3, t0 = 2 * p;
+      const bool z0 = t0 >= mt, z1 = t0 + 1 >= mt;
+#pragma unroll
+      for (int it = 0; it < D / 32; ++it) {
+        const int i0 = 4 * ((lane >> 2) + 8 * it);
+        const uint32_t r0 = z0 ? 0u : lds32(krow + t0 * RS + i0);
+        const uint32_t r1 = z1 ? 0u : lds32(krow + (t0 + 1) * RS + i0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kbf[(i0 + e) * 4 + p] = bf16x2_bits(sbyte(r0, e), sbyte(r1, e));
+      }
+    }
+  }
+
+  // ---- the folded readout: c = diag(beta) (I + L)^-T cq, y = G_m q - sum_t c_t G_t s_kt k_t, its digits
+  uint32_t yb[KS][2];                              // B fragments of the y digit rows (lanes g8 < 3)
+  float cvs = 0.0f;                                // c_s times the value scale (value coefficient of token s)
+  float wd0 = 0.0f, wd1 = 0.0f;                    // weights of the lane's two digit columns
+  if (has_token) {
+    const float kq = (65536.0f * qk[s & 7] + 256.0f * qk[8 + (s & 7)] + qk[16 + (s & 7)]) * sq;
+    float z = s < mt ? gmr * sk_s * kq : 0.0f;     // cq_s, then z_s of (I + L)^T z = cq
+#pragma unroll
+    for (int t = DF_TOK - 1; t >= 0; --t) {
+      if (t < mt) {
+        const float zt = __shfl_sync(0xffffffffu, z, t);
+        if (s < t) z = fmaf(-Lc[t], zt, z);
+      }
+    }
+    const float c_s = s < mt ? beta_s * z : 0.0f;
+    cvs = MX ? c_s : c_s * sv_s;
+    const float al = -c_s * Gs * sk_s;             // y = G_m q + sum_s al_s k_s (int8 codes)
+    float y[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) y[c] = Gm * tin.qx[c];
+#pragma unroll
+    for (int t = 0; t < DF_TOK; ++t) {
+      if (t < mt) {
+        const float at = __shfl_sync(0xffffffffu, al, t);
+        uint32_t kw;
+        if (CPL == 4) kw = lds32(krow + t * RS + 4 * lane);
+        else kw = *reinterpret_cast<const uint16_t *>(krow + t * RS + 2 * lane);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) y[c] = fmaf(at, sbyte(kw, c), y[c]);
+      }
+    }
+    float my = 0.0f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) my = fmaxf(my, fabsf(y[c]));
+    const float Ay = warp_max(my);
+    const float QMAX = 8323072.0f;
+    const bool yz = !(Ay >= FLT_MIN);
+    const float sy = yz ? 0.0f : __fdiv_rn(Ay, QMAX);
+    const float ry = yz ? 0.0f : __fdiv_rn(QMAX, Ay);
+    // keys of the lane: CPL*lane .. ; all in the first or all in the second half of a 16-key step
+    const float hs = ((CPL * lane) & 8) ? 0.0625f : 1.0f;
+    float dg[3][CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      const int yi = min(max(__float2int_rn(y[c] * ry), -8323072), 8323072);
+      const int y1 = (yi + 128) >> 8;
+      const int e2 = (y1 + 128) >> 8;
+      dg[0][c] = (float)e2 * hs;
+      dg[1][c] = (float)(y1 - (e2 << 8)) * hs;
+      dg[2][c] = (float)(yi - (y1 << 8)) * hs;
+    }
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      __half *row = ydig + d * YS + CPL * lane;
+      if constexpr (CPL == 4) {
+        const __half2 h0 = __floats2half2_rn(dg[d][0], dg[d][1]), h1 = __floats2half2_rn(dg[d][2], dg[d][3]);
+        *reinterpret_cast<uint2 *>(row) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1));
+      } else {
+        const __half2 h0 = __floats2half2_rn(dg[d][0], dg[d][1]);
+        *reinterpret_cast<__half2 *>(row) = h0;
+      }
+    }
+    wd0 = tq == 0 ? 65536.0f * sy : (tq == 1 ? sy : 0.0f);
+    wd1 = tq == 0 ? 256.0f * sy : 0.0f;
+    __syncwarp();
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      yb[ks][0] = g8 < 3 ? lds32(ydig + g8 * YS + 16 * ks + 2 * tq) : 0u;
+      yb[ks][1] = g8 < 3 ? lds32(ydig + g8 * YS + 16 * ks + 8 + 2 * tq) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) yb[ks][0] = yb[ks][1] = 0u;
+  }
+  // B fragments of the buffered keys (rounding step): token g8's keys as fp16, second halves / 16
+  uint32_t kb[KS][2];
+  if (do_flush) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint32_t x0 = g8 < mt ? lds32(krow + g8 * RS + 16 * ks + 4 * (tq >> 1)) : 0u;
+      const uint32_t x1 = g8 < mt ? lds32(krow + g8 * RS + 16 * ks + 8 + 4 * (tq >> 1)) : 0u;
+      const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;
+      kb[ks][0] = i8pair_f16(x0, sel, false);
+      kb[ks][1] = i8pair_f16(x1, sel, true);
+    }
+  }
+
+  // ---- group offsets: the contribution of the zero level (symmetric: code offset; zero point: 0) and, for zero
+  // points and int8 planes, the plain sums T2
+  float offy[NG][PL][2] = {}, t2y[NG][2] = {}, offk[NG][PL][2] = {}, t2k[NG][2] = {};
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+#pragma unroll
+    for (int pl = 0; pl < PL; ++pl) {
+      // int4 symmetric: every code at 8 -> -(T1 + 8 T2); int8 symmetric: low plane 0, high plane 8; zero point: 0
+      const uint32_t w = (!ZP && (BITS == 4 || pl == 1)) ? 0x88888888u : 0u;
+      if (has_token) df_offset<KSG>(w, yb + g * KSG, offy[g][pl]);
+      if (do_flush) df_offset<KSG>(w, kb + g * KSG, offk[g][pl]);
+    }
+    if (ZP) {
+      if (has_token) df_sum<KSG>(yb + g * KSG, t2y[g]);
+      if (do_flush) df_sum<KSG>(kb + g * KSG, t2k[g]);
+    }
+  }
+  // every warp's L2 prefetch of its remaining tiles, after the tables
+  if (MTW > 2 && lane < PL) {
+    constexpr uint32_t TW = NPP * 128;             // words of one M-tile in a plane
+    prefetch_l2(codes + lane * (D * D / 8) + (mt0 + 2) * TW, (MTW - 2) * TW * 4);
+  }
+
+  // ---- dots over the warp's M-tiles: o part (y digits) and, at a rounding, P_t (keys)
+#pragma unroll
+  for (int mi = 0; mi < MTW; ++mi) {
+    const int mtile = mt0 + mi;
+    uint32_t(&cw)[PL][NPP][4] = (mi & 1) ? cwB : cwA;
+    const int j0 = 16 * mtile + g8, j1 = j0 + 8;
+    float oc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // [column][digit] folded over groups
+    float pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // [column][token]
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float ay[PL][4], ak[PL][4];
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl) {
+        ay[pl][0] = ay[pl][2] = -offy[g][pl][0];
+        ay[pl][1] = ay[pl][3] = -offy[g][pl][1];
+        ak[pl][0] = ak[pl][2] = -offk[g][pl][0];
+        ak[pl][1] = ak[pl][3] = -offk[g][pl][1];
+      }
+#pragma unroll
+      for (int kk = 0; kk < KSG; ++kk) {
+        const int ks = g * KSG + kk;
+#pragma unroll
+        for (int pl = 0; pl < PL; ++pl) {
+          uint32_t a[4];
+          df_afrag<D, PL>(cw, pl, ks, a);
+          if (has_token) mma_f16(ay[pl], a, yb[ks][0], yb[ks][1]);
+          if (do_flush) mma_f16(ak[pl], a, kb[ks][0], kb[ks][1]);
+        }
+      }
+      // fold the group: exact integer level sums, times the group scale
+      const float s0 = __bfloat162float(ssc[g * D + j0]), s1 = __bfloat162float(ssc[g * D + j1]);
+      float z0 = 0.0f, z1 = 0.0f;
+      if (ZP) {
+        z0 = (float)szp[g * D + j0];
+        z1 = (float)szp[g * D + j1];
+      }
+      auto level = [&](const float (&x)[PL][4], int e, float zc, const float (&t2)[2]) -> float {
+        float v = PL == 2 ? fmaf(16.0f, x[PL - 1][e], x[0][e]) : x[0][e];
+        if (ZP) v = fmaf(-zc, t2[e & 1], v);
+        return v;
+      };
+      if (has_token) {
+        oc[0][0] = fmaf(s0, level(ay, 0, z0, t2y[g]), oc[0][0]);
+        oc[0][1] = fmaf(s0, level(ay, 1, z0, t2y[g]), oc[0][1]);
+        oc[1][0] = fmaf(s1, level(ay, 2, z1, t2y[g]), oc[1][0]);
+        oc[1][1] = fmaf(s1, level(ay, 3, z1, t2y[g]), oc[1][1]);
+      }
+      if (do_flush) {
+        pk[0][0] = fmaf(s0, level(ak, 0, z0, t2k[g]), pk[0][0]);
+        pk[0][1] = fmaf(s0, level(ak, 1, z0, t2k[g]), pk[0][1]);
+        pk[1][0] = fmaf(s1, level(ak, 2, z1, t2k[g]), pk[1][0]);
+        pk[1][1] = fmaf(s1, level(ak, 3, z1, t2k[g]), pk[1][1]);
+      }
+    }
+    // this tile's words are done with (the rounding reloads them from L2): the tile two ahead takes its registers
+    if (mi + 2 < MTW) df_load_tile<D, PL>(codes, mtile + 2, lane, cw);
+    if (has_token) {
+      float o0 = fmaf(wd1, oc[0][1], wd0 * oc[0][0]), o1 = fmaf(wd1, oc[1][1], wd0 * oc[1][0]);
+      o0 += __shfl_xor_sync(0xffffffffu, o0, 1);
+      o1 += __shfl_xor_sync(0xffffffffu, o1, 1);
+      if (tq == 0) po[j0] = o0;
+      else if (tq == 1) po[j1] = o1;
+    }
+    if (do_flush) {
+      const int t0 = 2 * tq;
+      if (t0 < mt) {
+        pb[t0 * D + j0] = pk[0][0];
+        pb[t0 * D + j1] = pk[1][0];
+      }
+      if (t0 + 1 < mt) {
+        pb[(t0 + 1) * D + j0] = pk[0][1];
+        pb[(t0 + 1) * D + j1] = pk[1][1];
+      }
+    }
+  }
+  __syncwarp();
+
+  // ---- output (lane: CPW consecutive columns of the warp's range): o = S_hat^T y + V^T c
+  const int jc = part * CW + CPW * lane;
+  if (has_token) {
+    float o[CPW];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) o[c] = po[jc + c];
+#pragma unroll
+    for (int t = 0; t < DF_TOK; ++t) {
+      if (t < mt) {
+        const float cv = __shfl_sync(0xffffffffu, cvs, t);
+        if (MX) {
+          const __nv_bfloat16 *vr = reinterpret_cast<const __nv_bfloat16 *>(vrow) + t * D + jc;
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) o[c] = fmaf(cv, __bfloat162float(vr[c]), o[c]);
+        } else {
+          const int8_t *vr = reinterpret_cast<const int8_t *>(vrow) + t * D + jc;
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) o[c] = fmaf(cv, (float)vr[c], o[c]);
+        }
+      }
+    }
+    store_io_vec<CPW>(io.o, (size_t)unit * D + jc, o, st.io);
+  }
+
+  if (do_flush) {
+    // ---- replay of the lane's columns: u_t = beta_t r_t - sum_{s<t} L_ts u_s, r_t = v_t - G_t s_kt P_t
+    float u[DF_TOK][CPW];
+#pragma unroll
+    for (int t = 0; t < DF_TOK; ++t) {
+      if (t < mt) {
+        const float4 tt = tk[t];
+        float acc[CPW];
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) {
+          const float v = MX ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(vrow)[t * D + jc + c])
+                             : tt.z * (float)reinterpret_cast<const int8_t *>(vrow)[t * D + jc + c];
+          acc[c] = tt.y * fmaf(-tt.x, pb[t * D + jc + c], v);
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) {
+          const float l = Lm[t * 8 + s2];
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) acc[c] = fmaf(-l, u[s2][c], acc[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) {
+          u[t][c] = acc[c];
+          pb[t * D + jc + c] = acc[c];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) u[t][c] = 0.0f;
+      }
+    }
+    __syncwarp();
+
+    // ---- rounding of the warp's M-tiles: S_new^T[j][i] = sum_s rho_s u_sj k_si + G_m s_gj (u_ij - z_gj)
+    const int dpp = 8;
+#pragma unroll 1
+    for (int mi = 0; mi < MTW; ++mi) {
+      const int mtile = mt0 + mi;
+      uint32_t cw[PL][NPP][4];
+      df_load_tile<D, PL>(codes, mtile, lane, cw);
+      // A: the three bf16 parts of rho_s u_s,j for tokens 2tq, 2tq + 1 and columns 16 mtile + g8, + 8
+      uint32_t ap[3][2];
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int j = 16 * mtile + g8 + 8 * hi, s0 = 2 * tq;
+        const float x0 = s0 < mt ? ckf[s0] * pb[s0 * D + j] : 0.0f;
+        const float x1 = s0 + 1 < mt ? ckf[s0 + 1] * pb[(s0 + 1) * D + j] : 0.0f;
+        const uint32_t p0 = bf16x2_bits(x0, x1);
+        const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
+        const uint32_t p1 = bf16x2_bits(r0, r1);
+        ap[0][hi] = p0;
+        ap[1][hi] = p1;
+        ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
+      }
+      const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        float fs[2], fz[2];
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int j = 16 * mtile + g8 + 8 * hi;
+          fs[hi] = Gm * __bfloat162float(ssc[gi * D + j]);
+          fz[hi] = -(8388608.0f + (float)(ZP ? (int)szp[gi * D + j] : OFF));
+        }
+        float c[NKG][4];
+#pragma unroll
+        for (int nn = 0; nn < NKG; ++nn) {
+          const uint32_t bk = kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + tq];
+          mma_bf16_z(c[nn], a16, bk, bk);
+          mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
+        }
+        // the old state: x = G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
+#pragma unroll
+        for (int nn = 0; nn < NKG; ++nn) {
+          const int nk = gi * NKG + nn, r = nk & 3;
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int wi = hi * 2 + ((nk >> 2) & 1);
+            uint32_t m16 = (cw[0][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu;
+            if (BITS == 8) m16 |= ((cw[PL - 1][nk >> 3][wi] >> (4 * r)) & 0x000F000Fu) << 4;
+            const float2 f = make_float2(__uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7610)),
+                                         __uint_as_float(__byte_perm(m16, 0x4B000000u, 0x7632)));
+            const float2 d = __fadd2_rn(f, make_float2(fz[hi], fz[hi]));
+            const float2 x = __ffma2_rn(make_float2(fs[hi], fs[hi]), d, make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]));
+            c[nn][2 * hi] = x.x;
+            c[nn][2 * hi + 1] = x.y;
+          }
+        }
+        // requantize the group for both columns; the lane's keys fill its own words
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          float sc;
+          int z;
+          if (!ZP) {
+            float A = 0.0f;
+#pragma unroll
+            for (int nn = 0; nn < NKG; ++nn) A = fmax3(A, fabsf(c[nn][2 * hi]), fabsf(c[nn][2 * hi + 1]));
+            A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 1));
+            A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 2));
+            constexpr float QMAX = (float)(OFF - 1);
+            sc = bf16_quot(A, QMAX, 1.0f / QMAX);
+            z = OFF;
+          } else {
+            float lo = 0.0f, hi_ = 0.0f;
+#pragma unroll
+            for (int nn = 0; nn < NKG; ++nn) {
+              lo = fmin3(lo, c[nn][2 * hi], c[nn][2 * hi + 1]);
+              hi_ = fmax3(hi_, c[nn][2 * hi], c[nn][2 * hi + 1]);
+            }
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+            hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 1));
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
+            hi_ = fmaxf(hi_, __shfl_xor_sync(0xffffffffu, hi_, 2));
+            constexpr float QM = (float)((1 << BITS) - 1);
+            sc = bf16_quot(__fsub_rn(hi_, lo), QM, 1.0f / QM);
+            z = 0;
+            if (sc >= FLT_MIN) z = min(max(__float2int_rn(__fmul_rn(-lo, rcp_bf16(sc))), 0), (1 << BITS) - 1);
+          }
+          if (!(sc >= FLT_MIN)) sc = 0.0f;
+          const float rr = sc > 0.0f ? rcp_bf16(sc) : 0.0f;
+          // codes: rint(x r) by the 1.5 * 2^23 rounding constant (symmetric: the clamp to +-qmax never binds,
+          // since s = bf16(A / qmax) puts |x r| below qmax + 1/2); zero point: + z, clamp to [0, 2^b - 1]
+          const float2 r2 = make_float2(rr, rr);
+          const float mg = ZP ? 12582912.0f : 12582912.0f + (float)OFF;
+          const float2 mg2 = make_float2(mg, mg);
+#pragma unroll
+          for (int pw = 0; pw < G / 32; ++pw) {
+            const int p = gi * (G / 32) + pw;      // 32-key span
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int r4 = 0; r4 < 4; ++r4) {
+              const int nn = 4 * pw + r4;
+              const float2 yv = __fadd2_rn(__fmul2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2), mg2);
+              uint32_t pair;
+              if (!ZP) {
+                pair = __byte_perm(__float_as_uint(yv.x), __float_as_uint(yv.y), 0x5410);   // bytes 1, 3 are 0
+                if (BITS == 4) {                   // each half is code + 8 in 1..15: no other bit is set
+                  w0 = r4 == 0 ? pair : w0 + (pair << (4 * r4));
+                  continue;
+                }
+              } else {
+                const int c0 = min(max((int)(__float_as_uint(yv.x) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
+                const int c1 = min(max((int)(__float_as_uint(yv.y) - 0x4B400000u) + z, 0), (1 << BITS) - 1);
+                pair = __byte_perm((uint32_t)c0, (uint32_t)c1, 0x5410);
+              }
+              w0 += (pair & 0x000F000Fu) << (4 * r4);
+              if (BITS == 8) w1 += ((pair >> 4) & 0x000F000Fu) << (4 * r4);
+            }
+            cw[0][p >> 1][hi * 2 + (p & 1)] = w0;
+            if (BITS == 8) cw[PL - 1][p >> 1][hi * 2 + (p & 1)] = w1;
+          }
+          if (tq == 0) {
+            const int j = 16 * mtile + g8 + 8 * hi;
+            scale[gi * D + j] = __float2bfloat16_rn(sc);
+            if (ZP) zpt[gi * D + j] = (uint8_t)z;
+          }
+        }
+      }
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl)
+#pragma unroll
+        for (int pp = 0; pp < NPP; ++pp)
+          *reinterpret_cast<uint4 *>(codes + pl * (D * D / 8) + ((mtile * NPP + pp) * 32 + lane) * 4) =
+              make_uint4(cw[pl][pp][0], cw[pl][pp][1], cw[pl][pp][2], cw[pl][pp][3]);
+    }
+  }
+  // every warp of the unit has read the count before it moves on
+  if (WU > 1) __syncthreads(); else __syncwarp();
+  if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
+}
+
+// One unit per block of WU warps; one launch per code pool (int4 heads, int8 heads).
+template <int D, int G, int BITS, int ZP, int MX, int WU>
+__global__ void __launch_bounds__(WU * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : 12) / WU)
+    decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_enter();
+  const int warp = threadIdx.x >> 5;
+  const int HP = BITS == 4 ? st.H4 : st.H8;
+  const int w = blockIdx.x;
+  if (w >= st.B * HP) return;
+  const int b = w / HP, slot = w - b * HP;
+  const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
+  const FoldSmem L = fold_smem(D, G, MX, ZP);
+  df_unit<D, G, BITS, ZP, MX, WU>(st, io, b, h, b * st.H + h, has_token, smem + (size_t)warp * L.total, warp);
+}
+
+template <int D, int G, int BITS, int ZP, int MX, int WU>
+static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, long units) {
+  const FoldSmem L = fold_smem(D, G, MX, ZP);
+  const size_t smem = (size_t)WU * L.total;
+  cudaError_t e = smem_opt_in<decode_fold_kernel<D, G, BITS, ZP, MX, WU>>(smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(WU * 32), smem, s, attr);
+  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU>, d, io, has_token);
+}
+
+// Warps per unit by the size of the pool: while the units fill fewer than a half (a quarter) of the SMs' warp
+// slots, two (four) warps share each unit and split its M-tiles, which shortens the per-unit chain.
+template <int D, int G, int BITS, int ZP, int MX>
+static cudaError_t launch_fold_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  const long units = (long)d.B * (BITS == 4 ? d.H4 : d.H8);
+  if (units == 0) return cudaSuccess;
+  const long slots = (long)device_sm_count() * 16;
+  if constexpr (D >= 128) {                      // (at least 32 columns per warp)
+    if (units * 4 <= slots) return launch_fold_w<D, G, BITS, ZP, MX, 4>(d, io, has_token, s, units);
+  }
+  if (units * 2 <= slots) return launch_fold_w<D, G, BITS, ZP, MX, 2>(d, io, has_token, s, units);
+  return launch_fold_w<D, G, BITS, ZP, MX, 1>(d, io, has_token, s, units);
+}
+
+template <int ZP, int MX>
+cudaError_t launch_fold_zm(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  cudaError_t e;
+  if (d.D == 128) {
+    if (d.G == 64) {
+      e = launch_fold_pool<128, 64, 4, ZP, MX>(d, io, has_token, s);
+      if (e == cudaSuccess) e = launch_fold_pool<128, 64, 8, ZP, MX>(d, io, has_token, s);
+    } else {
+      e = launch_fold_pool<128, 32, 4, ZP, MX>(d, io, has_token, s);
+      if (e == cudaSuccess) e = launch_fold_pool<128, 32, 8, ZP, MX>(d, io, has_token, s);
+    }
+  } else {
+    if (d.G == 64) {
+      e = launch_fold_pool<64, 64, 4, ZP, MX>(d, io, has_token, s);
+      if (e == cudaSuccess) e = launch_fold_pool<64, 64, 8, ZP, MX>(d, io, has_token, s);
+    } else {
+      e = launch_fold_pool<64, 32, 4, ZP, MX>(d, io, has_token, s);
+      if (e == cudaSuccess) e = launch_fold_pool<64, 32, 8, ZP, MX>(d, io, has_token, s);
+    }
+  }
+  return e;
+}
+extern template cudaError_t launch_fold_zm<0, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_fold_zm<0, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_fold_zm<1, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+extern template cudaError_t launch_fold_zm<1, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);
+
+}  // namespace pace

@@ -1418,34 +1418,18 @@ __global__ void __launch_bounds__(DM_WARPS * 32, BITS == 4 ? 4 : 3) decode_split
   if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
 }
 
-static int dm_sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 1;
-  }
-  return sms;
-}
-
 template <int D, int G, int BITS, int ZP, int MX>
 static cudaError_t launch_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, size_t unit_smem) {
-  static size_t opted = 0;
   const size_t smem = (size_t)DM_WARPS * unit_smem;   // the larger of the two launch shapes
-  if (smem > 48 * 1024 && smem > opted) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_mma_kernel<D, G, BITS, ZP, MX, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_split_kernel<D, G, BITS, ZP, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    opted = 227 * 1024;
-  }
+  cudaError_t e = smem_opt_in<decode_mma_kernel<D, G, BITS, ZP, MX, 1>>(smem);
+  if (e == cudaSuccess) e = smem_opt_in<decode_mma_kernel<D, G, BITS, ZP, MX, 2>>(smem);
+  if (e == cudaSuccess) e = smem_opt_in<decode_split_kernel<D, G, BITS, ZP, MX>>(smem);
+  if (e != cudaSuccess) return e;
   const long units = (long)d.B * (BITS == 4 ? d.H4 : d.H8);
   if (units == 0) return cudaSuccess;
   // one warp per unit while every SM holds 16 units' warps or more; below that, a CTA per unit
   cudaLaunchAttribute attr[1];
-  const long slots = (long)dm_sm_count() * 16;   // resident warps of the warp-level kernel
+  const long slots = (long)device_sm_count() * 16;   // resident warps of the warp-level kernel
   if (PACE_DM_CTA_PER_UNIT || (PACE_DM_WARPS_PER_UNIT == 0 && units * DM_WARPS <= slots)) {
     const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(DM_WARPS * 32), smem, s, attr);
     return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, BITS, ZP, MX>, d, io, has_token);

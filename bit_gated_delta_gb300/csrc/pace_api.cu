@@ -370,6 +370,13 @@ pace_status pace_state_import(pace_state *state, const void *src, size_t bytes, 
   return ok();
 }
 
+pace_status pace_test_wait_probe(pace_state *state, uint32_t ns) {
+  pace_status st = check_state(state);
+  if (st != PACE_OK) return st;
+  state->dev.probe_ns = ns;
+  return ok();
+}
+
 pace_status pace_get_status(const pace_state *state, int clear, int *status_out, void *stream) {
   pace_status st = check_state(state);
   if (st != PACE_OK) return st;

@@ -6,9 +6,43 @@
 #include <float.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pace_internal.h"
 
 namespace pace {
+
+// ---- host-side launch set-up, per device: the library may drive several GPUs, from several host threads
+constexpr int PACE_MAX_DEVICES = 64;
+inline int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= PACE_MAX_DEVICES) d = 0;
+  return d;
+}
+// SM count of the current device (queried once per device).
+inline int device_sm_count() {
+  static std::atomic<int> cache[PACE_MAX_DEVICES];
+  const int dev = current_device();
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+// Let kernel K use up to 227 KB of dynamic shared memory on the current device (once per kernel and device; a
+// racing second caller repeats the idempotent attribute call).
+template <auto K>
+inline cudaError_t smem_opt_in(size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  if (bytes > 227 * 1024) return cudaErrorInvalidValue;
+  static std::atomic<int> opted[PACE_MAX_DEVICES];
+  const int dev = current_device();
+  if (opted[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess) opted[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 // Sequential carving of a dynamic shared-memory block (16-byte aligned pieces, or `align`).
 __host__ __device__ inline size_t carve(size_t &off, size_t bytes, size_t align = 16) {

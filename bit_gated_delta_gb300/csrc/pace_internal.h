@@ -22,6 +22,8 @@ struct PaceDev {
   float *buf_s;            // [B][H][dP][4]: a, beta, s_k, s_v
   int32_t *m;              // [B][H]
   int32_t *status;         // one word: bit 0 set when a bounded device wait gave up
+  uint32_t probe_ns;       // failure-detection test: > 0 makes the tensor-core prefill wait this long on an
+                           // mbarrier that nothing signals, give up and report (pace_test_wait_probe)
   void *S;                 // f32 / bf16 [B][H][D][D]
   uint8_t head_is_int8[PACE_MAX_HEADS];
   int16_t head_slot[PACE_MAX_HEADS];
@@ -48,10 +50,6 @@ struct PaceIO {
 // Kernel launchers (each returns the launch status; nothing synchronises).
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
-// Quantized decode of the int4 heads of a d = 128 state with an int8 buffer and dP <= 8 on tcgen05, one thread
-// per state column (pace_decode_col_supported says whether a state qualifies).
-bool pace_decode_col_supported(const PaceDev &d);
-cudaError_t pace_launch_decode_col(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 // Tensor-core chunk prefill (d_k = d_v = 128, bf16 I/O); pace_prefill_tc_supported says whether it applies.

@@ -135,12 +135,8 @@ template <int D, int G>
 static cudaError_t launch_prefill_t(const PaceDev &d, const PaceIO &io, cudaStream_t s) {
   const size_t smem = prefill_smem_bytes(D);
   auto kern = prefill_kernel<D, G>;
-  static bool opted = false;
-  if (!opted) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    opted = true;
-  }
+  const cudaError_t e = smem_opt_in<prefill_kernel<D, G>>(smem);
+  if (e != cudaSuccess) return e;
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0 || io.n == 0) return cudaSuccess;
   kern<<<units, D, smem, s>>>(d, io);

@@ -47,7 +47,9 @@ constexpr uint32_t OFF_SC = OFF_WQ + T * T * 4;    // per token: a, beta, G_t, R
 constexpr uint32_t OFF_BAR = OFF_SC + 4 * T * 4;   // mbarrier
 constexpr uint32_t OFF_TB = OFF_BAR + 8;           // TMEM base address
 constexpr uint32_t OFF_OK = OFF_TB + 4;            // 1 while every wait succeeded
-constexpr uint32_t SMEM = OFF_OK + 4;
+constexpr uint32_t OFF_PROBE = OFF_OK + 4;         // mbarrier that nothing signals (failure-detection probe)
+constexpr uint32_t SMEM = OFF_PROBE + 8;
+static_assert(OFF_BAR % 8 == 0 && OFF_PROBE % 8 == 0, "mbarriers are 8-byte aligned");
 
 // Byte offset of element (row r, k) in a K-major operand with kdim columns made of 8-row x 16-byte cores:
 // cores adjacent along K (128 B apart), 8-row groups kdim/8 * 128 B apart.
@@ -166,8 +168,10 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     tmem_alloc(tbase, TMEM_COLS);
     tmem_relinquish();
   }
+  uint64_t *probe = reinterpret_cast<uint64_t *>(smem + OFF_PROBE);
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(probe, 1);
     mbar_fence_init();
     *okf = 1;
   }
@@ -220,7 +224,13 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
   if (n > 0) issue_rows(0);
 
   bool ok = true;
-  uint32_t pending = 0;                                 // parity of an MMA group whose wait gave up
+  bool drain = false;                                   // an MMA group whose wait gave up is still in flight
+  uint32_t pending = 0;                                 // its phase parity
+  if (st.probe_ns) {                                    // failure-detection probe: a wait that runs out, no MMA issued
+    if (tid == 0 && !mbar_wait(probe, 0, st.probe_ns)) *okf = 0;
+    __syncthreads();
+    if (!*okf) ok = false;
+  }
 #pragma unroll 1
   for (int t0 = 0; t0 < n && ok; t0 += T) {
     const int nt = min(T, n - t0);
@@ -292,6 +302,7 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     if (!*okf) {
       ok = false;
       pending = phase ^ 1u;
+      drain = true;
       break;
     }
     fence_after_sync();
@@ -420,6 +431,7 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     if (!*okf) {
       ok = false;
       pending = phase ^ 1u;
+      drain = true;
     }
     fence_after_sync();
   }
@@ -447,7 +459,7 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
     if (j == 0) st.m[unit] = 0;
   } else if (tid == 0) {
     atomicOr(st.status, 1);
-    mbar_wait(bar, pending, WAIT_NS);                   // let the MMAs in flight drain before TMEM is released
+    if (drain) mbar_wait(bar, pending, WAIT_NS);        // let the MMAs in flight drain before TMEM is released
   }
   asm volatile("cp.async.wait_all;" ::: "memory");      // no copy may land after the CTA leaves
   fence_before_sync();
@@ -457,12 +469,8 @@ __global__ void __launch_bounds__(ptc::NT, 1) prefill_tc_kernel(const PaceDev st
 
 template <int G>
 static cudaError_t launch_prefill_tc_t(const PaceDev &d, const PaceIO &io, cudaStream_t s) {
-  static bool opted = false;
-  if (!opted) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ptc::SMEM);
-    if (e != cudaSuccess) return e;
-    opted = true;
-  }
+  const cudaError_t e = smem_opt_in<prefill_tc_kernel<G>>(ptc::SMEM);
+  if (e != cudaSuccess) return e;
   const unsigned units = (unsigned)(d.B * d.H);
   if (units == 0 || io.n == 0) return cudaSuccess;
   prefill_tc_kernel<G><<<units, ptc::NT, ptc::SMEM, s>>>(d, io);

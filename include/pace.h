@@ -39,7 +39,7 @@ typedef enum {
   PACE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
   PACE_ERR_STATE = 3,        /* state handle cannot take this call (e.g. wrong mode) */
   PACE_ERR_CUDA = 4,         /* a CUDA call failed; see pace_last_error() */
-  PACE_ERR_TIMEOUT = 5       /* reserved: a bounded device wait gave up */
+  PACE_ERR_TIMEOUT = 5       /* a bounded device wait gave up (pace_get_status) */
 } pace_status;
 
 /* Resident state format. */
@@ -183,6 +183,13 @@ double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, i
  * (the unit involved was left unchanged). This call SYNCHRONISES `stream` to read the word; it returns
  * PACE_ERR_TIMEOUT when the bit is set, and clears it when `clear` is non-zero. */
 pace_status pace_get_status(const pace_state *state, int clear, int *status_out, void *stream);
+
+/* Failure-detection hook for tests (no fault, no hang): with ns > 0, every later tensor-core prefill launch of
+ * this state (d_k = d_v = 128, bf16 I/O) first waits on an mbarrier that nothing signals, for at most ns
+ * nanoseconds, gives up like any bounded wait that runs out: it issues no MMA, leaves every unit and its output
+ * unchanged, sets bit 0 of the status word (pace_get_status then returns PACE_ERR_TIMEOUT) and releases its
+ * tensor memory. ns = 0 turns the probe off. Host-only; PACE_ERR_INVALID_ARG for a NULL state. */
+pace_status pace_test_wait_probe(pace_state *state, uint32_t ns);
 
 /* Message for the last non-OK status returned to the calling thread ("" if none). */
 const char *pace_last_error(void);
