@@ -18,6 +18,8 @@
 // each column (four columns per lane) and requantizes the state per key-axis group as in decode_mma.cuh.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma.cuh"
 
 namespace pace {
@@ -25,7 +27,7 @@ namespace pace {
 constexpr int DF_TOK = 8;   // buffered tokens per unit this kernel handles (dP <= 8)
 
 struct FoldSmem {
-  size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, gram, qk, Lm, tk, ck, total;
+  size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, csx, gram, qk, Lm, tk, ck, total;
 };
 // Per-warp work area. int8 rows use a stride of D + 16 bytes and fp16 digit rows D + 8 halves, so that the
 // fragment loads of the eight rows of a tile fall in distinct banks.
@@ -34,13 +36,15 @@ __host__ __device__ inline FoldSmem fold_smem(int D, int G, int mixed, int zp) {
   size_t off = 0;
   L.krow = carve(off, (size_t)11 * (D + 16));               // key codes of tokens 0..7, then the 3 digits of q
   L.vrow = carve(off, (size_t)DF_TOK * D * (mixed ? 2 : 1)); // value codes (int8) or bf16 values
-  L.ydig = carve(off, (size_t)3 * (D + 8) * 2);              // fp16 digit rows of y
+  L.ydig = carve(off, (size_t)3 * (D + 8) * 2);              // fp16 digit rows of y; packed int4 keys of the
+                                                             // mixed buffer while staging
   L.ssc = carve(off, (size_t)(D / G) * D * 2);               // group scales (bf16), as resident
   L.szp = carve(off, zp ? (size_t)(D / G) * D : 0);          // zero points
   L.po = carve(off, (size_t)D * 4);                          // S_hat^T y per column
-  L.pb = carve(off, (size_t)DF_TOK * D * 4);                 // rounding step: P_t then u_t [t][j]; packed
-                                                             // int4 keys of the mixed buffer while staging
-  L.kbf = carve(off, (size_t)D * 4 * 4);                     // flush B operand: bf16 pairs of int8 keys [i][pair]
+  L.pb = carve(off, (size_t)DF_TOK * D * 4);                 // rounding step: P_t then u_t [t][j]
+  L.kbf = carve(off, (size_t)D * 4 * 4);                     // flush B operand: fp16 pairs of int8 keys [i][pair]
+  // steps without a rounding: the unit's int4 code words are staged over pb, kbf and this spare area
+  L.csx = carve(off, (size_t)D * D / 2 > (L.kbf - L.pb) + (size_t)D * 16 ? (size_t)D * D / 2 - (L.kbf - L.pb) - (size_t)D * 16 : 0);
   L.gram = carve(off, 64 * 4);                               // k_s.k_t (integers)
   L.qk = carve(off, 3 * 8 * 4);                              // (q digit d).k_t (integers)
   L.Lm = carve(off, 64 * 4);                                 // L[t][s]
@@ -186,13 +190,14 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   const int mt = m0 + has_token;
   const int do_flush = !has_token || mt == dP;
   const size_t ku = key_unit(st, unit);
+  const int mt0 = part * MTW;
   float4 bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);   // lane t < mt: token t's a, beta, key scale, value scale
   if (m0 > 0) {
     constexpr int rk = MX ? D / 2 : D, rv = MX ? 2 * D : D;
     const char *gk = static_cast<const char *>(st.buf_k) + ku * dP * rk;
     const char *gv = static_cast<const char *>(st.buf_v) + (size_t)unit * dP * rv;
     if (MX) {
-      unsigned char *scr = reinterpret_cast<unsigned char *>(pb);
+      unsigned char *scr = reinterpret_cast<unsigned char *>(ydig);
       for (int c = lane; c < m0 * rk / 16; c += 32) cp_async16(scr + 16 * c, gk + 16 * c);
     } else {
       for (int c = lane; c < m0 * (D / 16); c += 32) {
@@ -211,6 +216,11 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       for (int c = lane; c < NG * D / 16; c += 32) cp_async16(szp + 16 * c, gz + 16 * c);
     }
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // steps without a rounding stage the warp's int4 code words in shared memory (issued after the new token, below);
+  // the rounding step, whose work areas cover that space, keeps them in registers, two tiles ahead
+  const bool smem_codes = BITS == 4 && !do_flush;
+  const uint32_t *cs = reinterpret_cast<const uint32_t *>(pb);
 
   // ---- the new token: buffer slot m0 (global and shared), its scalars; q as three int8 digit rows
   float sq = 0.0f;                                 // scale of the q digits
@@ -265,8 +275,8 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     // q ~= sq (65536 d2 + 256 d1 + d0), balanced base-256 digits in [-128, 127] (rows 8, 9, 10)
     const float QMAX = 8323072.0f;
     const bool qz = !(Aq >= FLT_MIN);
-    sq = qz ? 0.0f : __fdiv_rn(Aq, QMAX);
-    const float rq = qz ? 0.0f : __fdiv_rn(QMAX, Aq);
+    sq = qz ? 0.0f : __fdividef(Aq, QMAX);       // internal digit scale: any sq ~ Aq/QMAX with rq ~ 1/sq works
+    const float rq = qz ? 0.0f : __fdividef(QMAX, Aq);
     int d2[CPL], d1[CPL], d0[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
@@ -280,15 +290,22 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     dm_store_bytes<CPL>(krow + 9 * RS + col0, d1);
     dm_store_bytes<CPL>(krow + 10 * RS + col0, d0);
   }
-  // the first two code tiles of this warp, once the new token is in
-  const int mt0 = part * MTW;
+  // the warp's first two code tiles, once the new token is in
   uint32_t cwA[PL][NPP][4], cwB[PL][NPP][4];
-  df_load_tile<D, PL>(codes, mt0, lane, cwA);
-  if (MTW > 1) df_load_tile<D, PL>(codes, mt0 + 1, lane, cwB);
-  cp_async_wait_all();
+  if (smem_codes) {
+#pragma unroll
+    for (int k = 0; k < MTW * NPP; ++k)
+      cp_async16(pb + (k * 32 + lane) * 4, codes + ((mt0 * NPP + k) * 32 + lane) * 4);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");    // the staging group (the codes may still land)
+  } else {
+    df_load_tile<D, PL>(codes, mt0, lane, cwA);
+    if (MTW > 1) df_load_tile<D, PL>(codes, mt0 + 1, lane, cwB);
+    cp_async_wait_all();
+  }
   __syncwarp();
   if (MX) {                                        // packed int4 keys (code + 8) -> int8 rows
-    const unsigned char *scr = reinterpret_cast<const unsigned char *>(pb);
+    const unsigned char *scr = reinterpret_cast<const unsigned char *>(ydig);
     for (int t = 0; t < m0; ++t) {
       if (lane < D / 8) {
         const uint32_t nb = *reinterpret_cast<const uint32_t *>(scr + t * (D / 2) + 4 * lane);
@@ -304,19 +321,25 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     __syncwarp();
   }
 
-  // ---- Gram products k_s.k_t and (q digit).k_t: integer MMA, A = [keys 0..7 | q digits] (M), B = keys (N)
+  // ---- Gram products k_s.k_t and (q digit).k_t: fp16 MMA (the int8 codes and digits are exact in fp16, every sum
+  // an exact integer below 2^24), A = [keys 0..7 | q digits] (M), B = keys (N). (An int8 MMA would take the codes as
+  // they are, but on this chip it runs at an eighth of the fp16 rate.)
   {
-    int gacc[4] = {0, 0, 0, 0};
+    float gacc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};   // two chains of the K steps
+    const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;   // the lane's key pair inside its 4-byte load
 #pragma unroll
-    for (int kb = 0; kb < D / 32; ++kb) {
-      const int off = 32 * kb + 4 * tq;
-      const uint32_t a0 = lds32(krow + g8 * RS + off), a2 = lds32(krow + g8 * RS + off + 16);
-      const uint32_t a1 = g8 < 3 ? lds32(krow + (8 + g8) * RS + off) : 0u;
-      const uint32_t a3 = g8 < 3 ? lds32(krow + (8 + g8) * RS + off + 16) : 0u;
-      imma_s8(gacc, a0, a1, a2, a3, a0, a2);
+    for (int ks = 0; ks < KS; ++ks) {
+      const int off = 16 * ks + 4 * (tq >> 1);
+      uint32_t a[4];
+      a[0] = i8pair_f16(lds32(krow + g8 * RS + off), sel, false);
+      a[2] = i8pair_f16(lds32(krow + g8 * RS + off + 8), sel, false);
+      a[1] = g8 < 3 ? i8pair_f16(lds32(krow + (8 + g8) * RS + off), sel, false) : 0u;
+      a[3] = g8 < 3 ? i8pair_f16(lds32(krow + (8 + g8) * RS + off + 8), sel, false) : 0u;
+      mma_f16(gacc[ks & 1], a, a[0], a[2]);
     }
-    *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2((float)gacc[0], (float)gacc[1]);
-    if (g8 < 3) *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2((float)gacc[2], (float)gacc[3]);
+    *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2(gacc[0][0] + gacc[1][0], gacc[0][1] + gacc[1][1]);
+    if (g8 < 3)
+      *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2(gacc[0][2] + gacc[1][2], gacc[0][3] + gacc[1][3]);
   }
   __syncwarp();
 
@@ -349,7 +372,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
       for (int t = 0; t < DF_TOK; ++t) Lm[t * 8 + s] = Lc[t];
     }
-    // the flush B operand: kbf[i][p] = bf16 pair (k_{2p,i}, k_{2p+1,i}), zero for tokens >= mt
+    // the flush B operand: kbf[i][p] = fp16 pair (k_{2p,i}, k_{2p+1,i}), zero for tokens >= mt
     {
       const int p = lane & 3, t0 = 2 * p;
       const bool z0 = t0 >= mt, z1 = t0 + 1 >= mt;
@@ -359,7 +382,10 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
         const uint32_t r0 = z0 ? 0u : lds32(krow + t0 * RS + i0);
         const uint32_t r1 = z1 ? 0u : lds32(krow + (t0 + 1) * RS + i0);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) kbf[(i0 + e) * 4 + p] = bf16x2_bits(sbyte(r0, e), sbyte(r1, e));
+        for (int e = 0; e < 4; ++e) {
+          const __half2 hk = __floats2half2_rn(sbyte(r0, e), sbyte(r1, e));
+          kbf[(i0 + e) * 4 + p] = *reinterpret_cast<const uint32_t *>(&hk);
+        }
       }
     }
   }
@@ -401,8 +427,8 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     const float Ay = warp_max(my);
     const float QMAX = 8323072.0f;
     const bool yz = !(Ay >= FLT_MIN);
-    const float sy = yz ? 0.0f : __fdiv_rn(Ay, QMAX);
-    const float ry = yz ? 0.0f : __fdiv_rn(QMAX, Ay);
+    const float sy = yz ? 0.0f : __fdividef(Ay, QMAX);
+    const float ry = yz ? 0.0f : __fdividef(QMAX, Ay);
     // keys of the lane: CPL*lane .. ; all in the first or all in the second half of a 16-key step
     const float hs = ((CPL * lane) & 8) ? 0.0625f : 1.0f;
     float dg[3][CPL];
@@ -469,87 +495,131 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       if (do_flush) df_sum<KSG>(kb + g * KSG, t2k[g]);
     }
   }
-  // every warp's L2 prefetch of its remaining tiles, after the tables
-  if (MTW > 2 && lane < PL) {
+
+  // the L2 prefetch of the warp's other tiles, after the tables (requested earlier, it delays the staging loads)
+  if (smem_codes) {
+    cp_async_wait_all();
+    __syncwarp();
+  } else if (MTW > 2 && lane < PL) {
     constexpr uint32_t TW = NPP * 128;             // words of one M-tile in a plane
     prefetch_l2(codes + lane * (D * D / 8) + (mt0 + 2) * TW, (MTW - 2) * TW * 4);
   }
 
-  // ---- dots over the warp's M-tiles: o part (y digits) and, at a rounding, P_t (keys)
+  // ---- dots over the warp's M-tiles: o part (y digits) and, at a rounding, P_t (keys). Two instantiations of the
+  // loop, so that a step without a rounding carries none of the rounding step's work.
+  auto dots = [&](auto with_keys) {
+    constexpr bool WK = decltype(with_keys)::value;
+    const bool wy = WK ? has_token != 0 : true;   // (steps without a rounding always have a token)
+    // TP tiles at a time (two on steps without a rounding, from registers cwA, cwB): their accumulators of every
+    // group are independent chains, issued interleaved so that the tensor pipe always has work from this warp (the
+    // rounding step, with twice the accumulators, takes one tile at a time)
+    constexpr int TP = 1;
+    static_assert(MTW % 2 == 0, "tiles are loaded in pairs");
 #pragma unroll
-  for (int mi = 0; mi < MTW; ++mi) {
-    const int mtile = mt0 + mi;
-    uint32_t(&cw)[PL][NPP][4] = (mi & 1) ? cwB : cwA;
-    const int j0 = 16 * mtile + g8, j1 = j0 + 8;
-    float oc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // [column][digit] folded over groups
-    float pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // [column][token]
+    for (int mi = 0; mi < MTW; mi += TP) {
+      float ay[TP][NG][PL][4], ak[TP][NG][PL][4];
 #pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      float ay[PL][4], ak[PL][4];
+      for (int tt = 0; tt < TP; ++tt)
 #pragma unroll
-      for (int pl = 0; pl < PL; ++pl) {
-        ay[pl][0] = ay[pl][2] = -offy[g][pl][0];
-        ay[pl][1] = ay[pl][3] = -offy[g][pl][1];
-        ak[pl][0] = ak[pl][2] = -offk[g][pl][0];
-        ak[pl][1] = ak[pl][3] = -offk[g][pl][1];
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+          for (int pl = 0; pl < PL; ++pl) {
+            ay[tt][g][pl][0] = ay[tt][g][pl][2] = -offy[g][pl][0];
+            ay[tt][g][pl][1] = ay[tt][g][pl][3] = -offy[g][pl][1];
+            if (WK) {
+              ak[tt][g][pl][0] = ak[tt][g][pl][2] = -offk[g][pl][0];
+              ak[tt][g][pl][1] = ak[tt][g][pl][3] = -offk[g][pl][1];
+            }
+          }
+      constexpr bool SM = !WK && BITS == 4;        // words from shared memory
+      if (SM) {
+#pragma unroll
+        for (int tt = 0; tt < TP; ++tt)
+#pragma unroll
+          for (int pp = 0; pp < NPP; ++pp) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(cs + (((mi + tt) * NPP + pp) * 32 + lane) * 4);
+            uint32_t(&w)[PL][NPP][4] = ((mi + tt) & 1) ? cwB : cwA;
+            w[0][pp][0] = v.x;
+            w[0][pp][1] = v.y;
+            w[0][pp][2] = v.z;
+            w[0][pp][3] = v.w;
+          }
       }
 #pragma unroll
-      for (int kk = 0; kk < KSG; ++kk) {
-        const int ks = g * KSG + kk;
+      for (int kk = 0; kk < KSG; ++kk)
 #pragma unroll
-        for (int pl = 0; pl < PL; ++pl) {
-          uint32_t a[4];
-          df_afrag<D, PL>(cw, pl, ks, a);
-          if (has_token) mma_f16(ay[pl], a, yb[ks][0], yb[ks][1]);
-          if (do_flush) mma_f16(ak[pl], a, kb[ks][0], kb[ks][1]);
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+          for (int tt = 0; tt < TP; ++tt) {
+            const int ks = g * KSG + kk;
+#pragma unroll
+            for (int pl = 0; pl < PL; ++pl) {
+              uint32_t a[4];
+              df_afrag<D, PL>(((mi + tt) & 1) ? cwB : cwA, pl, ks, a);
+              mma_f16(ay[tt][g][pl], a, yb[ks][0], yb[ks][1]);
+              if (WK) mma_f16(ak[tt][g][pl], a, kb[ks][0], kb[ks][1]);
+            }
+          }
+      // these tiles' words are done with (the rounding reloads them from L2): the tiles two ahead take their registers
+      if (!SM) {
+#pragma unroll
+        for (int tt = 0; tt < TP; ++tt)
+          if (mi + tt + 2 < MTW) df_load_tile<D, PL>(codes, mt0 + mi + tt + 2, lane, ((mi + tt) & 1) ? cwB : cwA);
+      }
+#pragma unroll
+      for (int tt = 0; tt < TP; ++tt) {
+        const int mtile = mt0 + mi + tt;
+        const int j0 = 16 * mtile + g8, j1 = j0 + 8;
+        float oc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // [column][digit] folded over groups
+        float pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};   // [column][token]
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          // fold the group: exact integer level sums, times the group scale
+          const float s0 = __bfloat162float(ssc[g * D + j0]), s1 = __bfloat162float(ssc[g * D + j1]);
+          float z0 = 0.0f, z1 = 0.0f;
+          if (ZP) {
+            z0 = (float)szp[g * D + j0];
+            z1 = (float)szp[g * D + j1];
+          }
+          auto level = [&](const float (&x)[PL][4], int e, float zc, const float (&t2)[2]) -> float {
+            float v = PL == 2 ? fmaf(16.0f, x[PL - 1][e], x[0][e]) : x[0][e];
+            if (ZP) v = fmaf(-zc, t2[e & 1], v);
+            return v;
+          };
+          oc[0][0] = fmaf(s0, level(ay[tt][g], 0, z0, t2y[g]), oc[0][0]);
+          oc[0][1] = fmaf(s0, level(ay[tt][g], 1, z0, t2y[g]), oc[0][1]);
+          oc[1][0] = fmaf(s1, level(ay[tt][g], 2, z1, t2y[g]), oc[1][0]);
+          oc[1][1] = fmaf(s1, level(ay[tt][g], 3, z1, t2y[g]), oc[1][1]);
+          if (WK) {
+            pk[0][0] = fmaf(s0, level(ak[tt][g], 0, z0, t2k[g]), pk[0][0]);
+            pk[0][1] = fmaf(s0, level(ak[tt][g], 1, z0, t2k[g]), pk[0][1]);
+            pk[1][0] = fmaf(s1, level(ak[tt][g], 2, z1, t2k[g]), pk[1][0]);
+            pk[1][1] = fmaf(s1, level(ak[tt][g], 3, z1, t2k[g]), pk[1][1]);
+          }
+        }
+        if (wy) {
+          float o0 = fmaf(wd1, oc[0][1], wd0 * oc[0][0]), o1 = fmaf(wd1, oc[1][1], wd0 * oc[1][0]);
+          o0 += __shfl_xor_sync(0xffffffffu, o0, 1);
+          o1 += __shfl_xor_sync(0xffffffffu, o1, 1);
+          if (tq == 0) po[j0] = o0;
+          else if (tq == 1) po[j1] = o1;
+        }
+        if (WK) {
+          const int t0 = 2 * tq;
+          if (t0 < mt) {
+            pb[t0 * D + j0] = pk[0][0];
+            pb[t0 * D + j1] = pk[1][0];
+          }
+          if (t0 + 1 < mt) {
+            pb[(t0 + 1) * D + j0] = pk[0][1];
+            pb[(t0 + 1) * D + j1] = pk[1][1];
+          }
         }
       }
-      // fold the group: exact integer level sums, times the group scale
-      const float s0 = __bfloat162float(ssc[g * D + j0]), s1 = __bfloat162float(ssc[g * D + j1]);
-      float z0 = 0.0f, z1 = 0.0f;
-      if (ZP) {
-        z0 = (float)szp[g * D + j0];
-        z1 = (float)szp[g * D + j1];
-      }
-      auto level = [&](const float (&x)[PL][4], int e, float zc, const float (&t2)[2]) -> float {
-        float v = PL == 2 ? fmaf(16.0f, x[PL - 1][e], x[0][e]) : x[0][e];
-        if (ZP) v = fmaf(-zc, t2[e & 1], v);
-        return v;
-      };
-      if (has_token) {
-        oc[0][0] = fmaf(s0, level(ay, 0, z0, t2y[g]), oc[0][0]);
-        oc[0][1] = fmaf(s0, level(ay, 1, z0, t2y[g]), oc[0][1]);
-        oc[1][0] = fmaf(s1, level(ay, 2, z1, t2y[g]), oc[1][0]);
-        oc[1][1] = fmaf(s1, level(ay, 3, z1, t2y[g]), oc[1][1]);
-      }
-      if (do_flush) {
-        pk[0][0] = fmaf(s0, level(ak, 0, z0, t2k[g]), pk[0][0]);
-        pk[0][1] = fmaf(s0, level(ak, 1, z0, t2k[g]), pk[0][1]);
-        pk[1][0] = fmaf(s1, level(ak, 2, z1, t2k[g]), pk[1][0]);
-        pk[1][1] = fmaf(s1, level(ak, 3, z1, t2k[g]), pk[1][1]);
-      }
     }
-    // this tile's words are done with (the rounding reloads them from L2): the tile two ahead takes its registers
-    if (mi + 2 < MTW) df_load_tile<D, PL>(codes, mtile + 2, lane, cw);
-    if (has_token) {
-      float o0 = fmaf(wd1, oc[0][1], wd0 * oc[0][0]), o1 = fmaf(wd1, oc[1][1], wd0 * oc[1][0]);
-      o0 += __shfl_xor_sync(0xffffffffu, o0, 1);
-      o1 += __shfl_xor_sync(0xffffffffu, o1, 1);
-      if (tq == 0) po[j0] = o0;
-      else if (tq == 1) po[j1] = o1;
-    }
-    if (do_flush) {
-      const int t0 = 2 * tq;
-      if (t0 < mt) {
-        pb[t0 * D + j0] = pk[0][0];
-        pb[t0 * D + j1] = pk[1][0];
-      }
-      if (t0 + 1 < mt) {
-        pb[(t0 + 1) * D + j0] = pk[0][1];
-        pb[(t0 + 1) * D + j1] = pk[1][1];
-      }
-    }
-  }
+  };
+  if (do_flush) dots(std::true_type{});
+  else dots(std::false_type{});
   __syncwarp();
 
   // ---- output (lane: CPW consecutive columns of the warp's range): o = S_hat^T y + V^T c
@@ -610,24 +680,43 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 
     // ---- rounding of the warp's M-tiles: S_new^T[j][i] = sum_s rho_s u_sj k_si + G_m s_gj (u_ij - z_gj)
     const int dpp = 8;
+    uint32_t cwn[PL][NPP][4];                      // the next tile's words, requested one tile ahead
+    df_load_tile<D, PL>(codes, mt0, lane, cwn);
 #pragma unroll 1
     for (int mi = 0; mi < MTW; ++mi) {
       const int mtile = mt0 + mi;
       uint32_t cw[PL][NPP][4];
-      df_load_tile<D, PL>(codes, mtile, lane, cw);
-      // A: the three bf16 parts of rho_s u_s,j for tokens 2tq, 2tq + 1 and columns 16 mtile + g8, + 8
-      uint32_t ap[3][2];
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl)
+#pragma unroll
+        for (int pp = 0; pp < NPP; ++pp)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) cw[pl][pp][e] = cwn[pl][pp][e];
+      if (mi + 1 < MTW) df_load_tile<D, PL>(codes, mtile + 1, lane, cwn);
+      // A: rho_s u_s,j for tokens 2tq, 2tq + 1 and columns 16 mtile + g8, + 8, times a power of two 2^e_j per column
+      // that puts the column's largest |rho_s u_s,j| in [2^8, 2^9), as two fp16 parts (about 22 significant bits;
+      // K = 16 = 8 tokens x 2 parts, one MMA per key tile). The old state is scaled by the same 2^e_j, so the
+      // accumulator holds 2^e_j x; scales and codes are invariant under it (the scale found is divided back).
+      uint32_t ap[2][2];
+      float pw2[2], pw2i[2];
 #pragma unroll
       for (int hi = 0; hi < 2; ++hi) {
         const int j = 16 * mtile + g8 + 8 * hi, s0 = 2 * tq;
-        const float x0 = s0 < mt ? ckf[s0] * pb[s0 * D + j] : 0.0f;
-        const float x1 = s0 + 1 < mt ? ckf[s0 + 1] * pb[(s0 + 1) * D + j] : 0.0f;
-        const uint32_t p0 = bf16x2_bits(x0, x1);
-        const float r0 = x0 - bf16_lo(p0), r1 = x1 - bf16_hi(p0);
-        const uint32_t p1 = bf16x2_bits(r0, r1);
-        ap[0][hi] = p0;
-        ap[1][hi] = p1;
-        ap[2][hi] = bf16x2_bits(r0 - bf16_lo(p1), r1 - bf16_hi(p1));
+        float x0 = s0 < mt ? ckf[s0] * pb[s0 * D + j] : 0.0f;
+        float x1 = s0 + 1 < mt ? ckf[s0 + 1] * pb[(s0 + 1) * D + j] : 0.0f;
+        float mx = fmaxf(fabsf(x0), fabsf(x1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const int e = min(max(135 - (int)((__float_as_uint(mx) >> 23) & 0xFFu), -60), 60);
+        pw2[hi] = __uint_as_float((uint32_t)(e + 127) << 23);
+        pw2i[hi] = __uint_as_float((uint32_t)(127 - e) << 23);
+        x0 *= pw2[hi];
+        x1 *= pw2[hi];
+        const __half2 p0 = __floats2half2_rn(x0, x1);
+        const float2 f0 = __half22float2(p0);
+        const __half2 p1 = __floats2half2_rn(x0 - f0.x, x1 - f0.y);
+        ap[0][hi] = *reinterpret_cast<const uint32_t *>(&p0);
+        ap[1][hi] = *reinterpret_cast<const uint32_t *>(&p1);
       }
       const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
 #pragma unroll
@@ -636,17 +725,16 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
         for (int hi = 0; hi < 2; ++hi) {
           const int j = 16 * mtile + g8 + 8 * hi;
-          fs[hi] = Gm * __bfloat162float(ssc[gi * D + j]);
+          fs[hi] = Gm * __bfloat162float(ssc[gi * D + j]) * pw2[hi];
           fz[hi] = -(8388608.0f + (float)(ZP ? (int)szp[gi * D + j] : OFF));
         }
         float c[NKG][4];
 #pragma unroll
         for (int nn = 0; nn < NKG; ++nn) {
           const uint32_t bk = kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + tq];
-          mma_bf16_z(c[nn], a16, bk, bk);
-          mma8_bf16(c[nn], ap[2][0], ap[2][1], bk);
+          mma_f16_z(c[nn], a16, bk, bk);
         }
-        // the old state: x = G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
+        // the old state: 2^e_j x = 2^e_j G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
 #pragma unroll
         for (int nn = 0; nn < NKG; ++nn) {
           const int nk = gi * NKG + nn, r = nk & 3;
@@ -691,12 +779,16 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
             constexpr float QM = (float)((1 << BITS) - 1);
             sc = bf16_quot(__fsub_rn(hi_, lo), QM, 1.0f / QM);
             z = 0;
-            if (sc >= FLT_MIN) z = min(max(__float2int_rn(__fmul_rn(-lo, rcp_bf16(sc))), 0), (1 << BITS) - 1);
+            if (sc * pw2i[hi] >= FLT_MIN) z = min(max(__float2int_rn(__fmul_rn(-lo, rcp_bf16(sc))), 0), (1 << BITS) - 1);
           }
-          if (!(sc >= FLT_MIN)) sc = 0.0f;
+          // sc is 2^e_j times the scale (bf16-exact either way); a zero or subnormal scale makes the group zero
+          float st = sc * pw2i[hi];
+          if (!(st >= FLT_MIN)) st = sc = 0.0f;
           const float rr = sc > 0.0f ? rcp_bf16(sc) : 0.0f;
-          // codes: rint(x r) by the 1.5 * 2^23 rounding constant (symmetric: the clamp to +-qmax never binds,
-          // since s = bf16(A / qmax) puts |x r| below qmax + 1/2); zero point: + z, clamp to [0, 2^b - 1]
+          // codes: rint(x r) by the 1.5 * 2^23 rounding constant, one fused multiply-add (the product is not
+          // rounded first; it differs from rint(fl(x r)) only within 2^-24 of a half-integer) (symmetric: the clamp
+          // to +-qmax never binds, since s = bf16(A / qmax) puts |x r| below qmax + 1/2); zero point: + z, clamp
+          // to [0, 2^b - 1]
           const float2 r2 = make_float2(rr, rr);
           const float mg = ZP ? 12582912.0f : 12582912.0f + (float)OFF;
           const float2 mg2 = make_float2(mg, mg);
@@ -707,7 +799,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
             for (int r4 = 0; r4 < 4; ++r4) {
               const int nn = 4 * pw + r4;
-              const float2 yv = __fadd2_rn(__fmul2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2), mg2);
+              const float2 yv = __ffma2_rn(make_float2(c[nn][2 * hi], c[nn][2 * hi + 1]), r2, mg2);
               uint32_t pair;
               if (!ZP) {
                 pair = __byte_perm(__float_as_uint(yv.x), __float_as_uint(yv.y), 0x5410);   // bytes 1, 3 are 0
@@ -728,7 +820,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
           }
           if (tq == 0) {
             const int j = 16 * mtile + g8 + 8 * hi;
-            scale[gi * D + j] = __float2bfloat16_rn(sc);
+            scale[gi * D + j] = __float2bfloat16_rn(st);
             if (ZP) zpt[gi * D + j] = (uint8_t)z;
           }
         }
