@@ -50,6 +50,9 @@ def parse_args(argv=None):
     return p.parse_args(argv)
 
 
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e datasheet bandwidth (context beside the measured copy peak)
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -58,6 +61,15 @@ def read_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def read_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (a kernel timed inside a long run), measured, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
 
 
 class ClockSampler:
@@ -150,8 +162,8 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode_mma.cuh", "bit_gated_delta_gb300/csrc/decode_mma_s8.cu",
-                  "bit_gated_delta_gb300/csrc/decode_col.cu", "bit_gated_delta_gb300/csrc/pace_common.cuh",
+DECODE_SOURCES = ["bit_gated_delta_gb300/csrc/decode_fold.cuh", "bit_gated_delta_gb300/csrc/decode_fold_s8.cu",
+                  "bit_gated_delta_gb300/csrc/decode_mma.cuh", "bit_gated_delta_gb300/csrc/pace_common.cuh",
                   "bit_gated_delta_gb300/csrc/pace_internal.h"]
 
 
@@ -178,14 +190,15 @@ class DecodeSetup:
 
     NI = 8
 
-    def __init__(self, P, torch, wl, state_mode, R, prefill_tokens=512):
+    def __init__(self, P, torch, wl, state_mode, R, prefill_tokens=512, mask=None):
         import synth
         self.P, self.torch, self.wl = P, torch, wl
         bf16 = state_mode == P.PACE_STATE_BF16
         self.cfg = P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, zero_point=wl.zero_point,
                                  buf_mode=P.PACE_BUF_MIXED if wl.mixed_buffer else P.PACE_BUF_INT8,
                                  state_mode=state_mode)
-        self.states = [P.PaceState(self.cfg, wl.B) for _ in range(R)]
+        self.states = [P.PaceState(self.cfg, wl.B, mask) for _ in range(R)]
+        self.uses = [0] * R              # decode steps launched on each set (its buffer phase, mod dP)
         self.R = R
         o = torch.empty(wl.B, wl.H, 256, wl.d_v, dtype=torch.bfloat16, device="cuda")
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -218,6 +231,23 @@ class DecodeSetup:
     def step_on(self, st, i, stream=None):
         x = self.inputs[i % self.NI]
         st.decode_step(x["q"], x["k"], x["v"], x["a"], x["beta"], self.o, stream)
+        self.uses[self.states.index(st)] += 1
+
+    def replayed(self, n_steps):
+        """Account the launches of one replay of a graph of n_steps steps."""
+        for i in range(n_steps):
+            self.uses[i % self.R] += 1
+
+    def rounding_steps(self, n_steps):
+        """How many of the next n_steps steps (sets in rotation) are rounding steps."""
+        uses = list(self.uses)
+        n = 0
+        for i in range(n_steps):
+            r = i % self.R
+            if uses[r] % self.wl.dP == self.wl.dP - 1:
+                n += 1
+            uses[r] += 1
+        return n
 
     def graph(self, n_steps):
         """A CUDA graph of n_steps consecutive decode steps over the rotating sets."""
@@ -230,9 +260,11 @@ class DecodeSetup:
                 self.step_on(self.states[i % self.R], i)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+        uses = list(self.uses)
         with torch.cuda.graph(g):
             for i in range(n_steps):
                 self.step_on(self.states[i % self.R], i)
+        self.uses = uses                 # capture launches nothing
         return g
 
     def close(self):
@@ -247,9 +279,11 @@ def time_steps(torch, setup, K, W, sampler=None):
     g = setup.graph(G)
     for _ in range((W + G - 1) // G):
         g.replay()
+        setup.replayed(G)
     tail = K % G
     gt = setup.graph(tail) if tail else None
     torch.cuda.synchronize()
+    setup.window_roundings = setup.rounding_steps(K)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ctx = sampler if sampler is not None else _Null()
     with ctx:
@@ -313,8 +347,16 @@ def time_e2e(torch, P, setup, K):
     ev1.record()
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1) / n
+    # the host-to-device copy alone, the same packed pinned buffers back to back: the rate that bounds the leg
+    ev0.record()
+    for i in range(n):
+        dbuf.copy_(host[i % DecodeSetup.NI], non_blocking=True)
+    ev1.record()
+    torch.cuda.synchronize()
+    ms_copy = ev0.elapsed_time(ev1) / n
     return {"value": wl.B / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "steps": n, "note": "one packed host-to-device copy per step"}
+            "ms_per_step": ms, "steps": n, "note": "one packed host-to-device copy per step",
+            "h2d_copy_alone_ms": ms_copy, "h2d_copy_alone_gbs": total / (ms_copy * 1e-3) / 1e9}
 
 
 # ------------------------------------------------------------------------------------------------------
@@ -350,6 +392,58 @@ def oracle_decode_rate(wl, budget_s: float, n_units: int = 32):
     return {"value": tokens_per_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{n_units} heads of one sequence, 512-token prefill, {steps} decode steps "
                       f"({steps // wl.dP} periods), {el:.1f} s; tokens/s = unit-steps/s / {wl.H} heads"}
+
+
+def oracle_rate(wl, n_units: int, budget_s: float, threads: int, prefill: int = 256, int8_heads=()):
+    """Decode unit-steps/s of the CPU oracle: n_units heads of one sequence (heads listed in int8_heads kept at
+    8 bits), `prefill` tokens of prefill, then whole decode periods until the budget is used."""
+    import oracle as O
+    import synth
+    wl1 = wl.with_(B=1, H=n_units)
+    buf = O.BUF_MIXED if wl.mixed_buffer else O.BUF_INT8
+    units = [O.Unit(O.Cfg(d_k=wl.d_k, d_v=wl.d_v, g=wl.g, bits=8 if h in int8_heads else 4,
+                          zero_point=wl.zero_point, dP=wl.dP, buf_mode=buf)) for h in range(n_units)]
+    for t0 in range(0, prefill, 256):
+        x = synth.chunk_inputs(wl1, t0, min(256, prefill - t0))
+        for h, u in enumerate(units):
+            O.prefill(u, x["q"][0, h], x["k"][0, h], x["v"][0, h], x["a"][0, h], x["beta"][0, h])
+    toks = [synth.token_inputs(wl1, prefill + i) for i in range(wl.dP)]
+    groups = [[h for h in range(n_units) if (h in int8_heads) == b] for b in (False, True)]
+    steps, t_start = 0, time.perf_counter()
+    while True:
+        for i in range(wl.dP):
+            x = toks[i]
+            for hs in groups:
+                if hs:
+                    O.decode_batch([units[h] for h in hs], x["q"][0, hs], x["k"][0, hs], x["v"][0, hs], x["a"][0, hs],
+                                   x["beta"][0, hs], nthreads=threads)
+        steps += wl.dP
+        el = time.perf_counter() - t_start
+        if el >= budget_s:
+            break
+    return n_units * steps / el, steps, el
+
+
+def oracle_rates(budget_s: float = 1.5):
+    """The CPU oracle on configs 0-3, one thread and all cores (bounded samples; tokens/s of the whole
+    configuration = unit-steps/s / units per token)."""
+    import oracle as O
+    import synth
+    cores = O.max_threads()
+    out = {"cores": cores}
+    cases = [("tiny", synth.workload("tiny"), 4, 4, 256, ()),              # all 4 units (2 sequences x 2 heads)
+             ("pace4", synth.workload("pace4"), 32, 32, 256, ()),
+             ("pace48", synth.workload("pace48"), 32, 32, 256, tuple(range(0, 32, 4))),
+             ("sweep_24x16", synth.workload("sweep"), 16, 24 * 16, 256, ())]
+    for name, wl, n, per_token, pf, i8 in cases:
+        row = {}
+        for th in (1, cores):
+            ups, steps, el = oracle_rate(wl, n, budget_s, th, pf, i8)
+            row[f"tokens_per_s_{th}t"] = ups / per_token
+        row["sample"] = (f"{n} units of one sequence ({len(i8)} at 8 bits), {pf}-token prefill, decode periods for "
+                         f"{budget_s} s per thread count; one token of the configuration = {per_token} unit-steps")
+        out[name] = row
+    return out
 
 
 def run_reference(args):
@@ -389,14 +483,16 @@ def rotation_count(nbytes: int, dP: int, align_dp: bool) -> int:
     return int(R)
 
 
-def measure(P, torch, wl, state_mode, K, W, sampler=None, min_sets=2):
+def measure(P, torch, wl, state_mode, K, W, sampler=None, min_sets=2, mask=None):
     bytes1 = P.pace_state_bytes(P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, state_mode=state_mode,
-                                              buf_mode=P.PACE_BUF_INT8))
+                                              zero_point=wl.zero_point,
+                                              buf_mode=P.PACE_BUF_MIXED if wl.mixed_buffer else P.PACE_BUF_INT8),
+                                mask)
     periodic = state_mode in (P.PACE_STATE_QUANT, P.PACE_STATE_BF16_BUF)
     R = max(rotation_count(bytes1, wl.dP, periodic), min_sets)
     if periodic:
         R = -(-R // wl.dP) * wl.dP
-    setup = DecodeSetup(P, torch, wl, state_mode, R)
+    setup = DecodeSetup(P, torch, wl, state_mode, R, mask=mask)
     ms = time_steps(torch, setup, K, W, sampler)
     return setup, ms, R
 
@@ -456,8 +552,11 @@ def prefill_longctx(P, torch, n_tokens=32768, distinct=8):
     # per 32-token sub-chunk: S^T [k|q] (2 parts, 128x64x128), Gram (128x32x128), update (2 parts, 128x128x32)
     flop_sub = 2 * (2 * 128 * 64 * 128 + 128 * 32 * 128 + 2 * 128 * 128 * 32)
     tflops = units * n_chunks * 8 * flop_sub / (ms * 1e-3) / 1e12
+    tpk, tpk_kind = read_tensor_peak()
     return {"B": wl.B, "H": wl.H, "d": wl.d_k, "tokens": n_tokens, "chunks": n_chunks, "ms": ms,
             "tokens_per_s": wl.B * n_tokens / (ms * 1e-3), "tensor_tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tpk, "unit": "TFLOP/s", "frac": tflops / tpk,
+                         "peak_kind": f"{tpk_kind} bf16 dense, sustained", "kernel": "pace::prefill_tc_kernel<64>"},
             "note": "tensor-core chunk prefill; inputs drawn on the device, 8 distinct chunks reused"}
 
 
@@ -510,6 +609,57 @@ def synthetic_error_study(P, torch, prefill_tokens=32768, decode_tokens=1024):
                                           "min": float(ratio.min()), "heads_key_axis_lower": float(np.mean(ratio > 1))},
             "drift_vs_unquantized": drift,
             "note": "fp32 unquantized reference vs PACE-4 (g=64, int8 buffer) at dP 1/8/32; bf16 outputs"}
+
+
+def pace48_leg(P, torch, peak, K, W):
+    """PACE-4/8 (BASELINE config 2): batch 128, 32 heads, g = 32 with integer zero points, mixed decode buffer (int4
+    keys, bf16 values); the quarter of heads with the largest E_h = e_h / (1 - a_h^(2 dP)) stay int8, chosen by
+    pace_assign_heads from the GPU calibration of a 512-token fp32 prefill (e_h averaged over the sequences).
+    Algorithmic bytes per unit-step as resident (u8 zero points), averaged over the 24 int4 and 8 int8 heads."""
+    import synth
+    wl = synth.workload("pace48")
+    a_h = synth.head_decays(wl)
+    cfg = P.make_config(wl.H, wl.d_k, wl.B, dP=wl.dP, group=wl.g, zero_point=1, state_mode=P.PACE_STATE_FP32,
+                        buf_mode=P.PACE_BUF_FP32)
+    st = P.PaceState(cfg, wl.B)
+    o = torch.empty(wl.B, wl.H, 256, wl.d_v, dtype=torch.bfloat16, device="cuda")
+    for c in range(2):
+        x = synth.device_chunk_inputs(wl, 256 * c, 256)
+        st.prefill_chunk(x["q"], x["k"], x["v"], x["a"], x["beta"], o)
+    e = torch.zeros(wl.B * wl.H, device="cuda")
+    P.pace_calib_error_energy(st.handle, 4, wl.g, 1, e)
+    e_h = e.view(wl.B, wl.H).mean(0).cpu().numpy()
+    st.close()
+    mask = P.pace_assign_heads(e_h, a_h, wl.dP, 0.25)
+    s, ms, R = measure(P, torch, wl, P.PACE_STATE_QUANT, K, W, mask=mask)
+    rounding = s.window_roundings
+    s.close()
+    n8 = int(mask.sum())
+    per = ((wl.H - n8) * decode_bytes_period_avg(wl.d_k, wl.g, wl.dP, zp=1, bits=4, mixed=1) +
+           n8 * decode_bytes_period_avg(wl.d_k, wl.g, wl.dP, zp=1, bits=8, mixed=1)) / wl.H
+    alg = wl.B * wl.H * per
+    return {"B": wl.B, "H": wl.H, "int8_heads": [int(h) for h in np.flatnonzero(mask)], "tokens_per_s": wl.B / (ms * 1e-3),
+            "ms_per_step": ms, "bytes_per_unit_step": per, "achieved_gbs": alg / (ms * 1e-3) / 1e9,
+            "frac": alg / (ms * 1e-3) / 1e9 / peak, "rotating_sets": R, "rounding_steps_in_window": rounding,
+            "steps": K, "note": "two launches per step (int4 pool, int8 pool)"}
+
+
+def longctx_decode(P, torch, peak, K, W):
+    """Decode of the long-context shape (48 heads, d=128, batch 16, PACE-4 g=64) at rounding periods dP = 1, 8, 32,
+    after a 512-token prefill (the decode cost does not depend on the context length: the state has a fixed size);
+    rotating state sets as in the default line. dP <= 8 runs the folded-readout kernel, dP = 32 the general one."""
+    import synth
+    out = {}
+    for dP in (1, 8, 32):
+        wl = synth.workload("longctx").with_(dP=dP)
+        k = -(-K // dP) * dP
+        s, ms, R = measure(P, torch, wl, P.PACE_STATE_QUANT, k, W)
+        s.close()
+        alg = wl.B * wl.H * decode_bytes_period_avg(wl.d_k, wl.g, dP)
+        out[f"dP{dP}"] = {"tokens_per_s": wl.B / (ms * 1e-3), "ms_per_step": ms, "achieved_gbs": alg / (ms * 1e-3) / 1e9,
+                          "frac": alg / (ms * 1e-3) / 1e9 / peak, "rotating_sets": R, "steps": k}
+        torch.cuda.empty_cache()
+    return out
 
 
 def shared_key_heads(P, torch, peak, B=64, H=32, Hk=16, steps=2000):
@@ -609,11 +759,14 @@ def main():
     units = wl.B * wl.H
     alg = units * decode_bytes_period_avg(wl.d_k, wl.g, wl.dP)
     achieved = alg / (ms * 1e-3) / 1e9
-    traffic = recorded_traffic("decode_mma_kernel", f"pace4_b{wl.B}")
+    traffic = recorded_traffic("decode_fold_kernel", f"pace4_b{wl.B}")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_mma_kernel<128,64,4>",
+                "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS,
+                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_fold_kernel<128,64,4,0,0,1>",
                 "algorithmic_bytes_per_launch": alg,
-                "note": "one decode_mma_kernel launch per step; duration = event time of K graph-replayed steps / K"}
+                "note": "one decode_fold_kernel launch per step; duration = event time of K graph-replayed steps / K; "
+                        "algorithmic bytes averaged over a rounding period"}
+    rounding = setup.window_roundings
     e2e = time_e2e(torch, P, setup, K)
     e2e["value"] *= world
     prefill = {"tokens": setup.prefill_tokens, "ms": setup.prefill_ms,
@@ -649,14 +802,19 @@ def main():
         extra["prefill_longctx"] = prefill_longctx(P, torch)
         extra["synthetic_error"] = synthetic_error_study(P, torch)
         extra["pace4_shared_keys_b64"] = shared_key_heads(P, torch, peak)
+        extra["pace48_b128"] = pace48_leg(P, torch, peak, k2, max(3, W // 4))
+        extra["longctx_decode"] = longctx_decode(P, torch, peak, k2, max(3, W // 4))
 
     cb = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         cb = oracle_decode_rate(wl, args.cpu_seconds)
+        if args.extra:
+            cb["configs"] = oracle_rates()
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
                 "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32", "data": "synthetic", "config": workload_config(wl, R),
+                "dtype": "f32", "data": "synthetic", "config": {**workload_config(wl, R),
+                                                              "rounding_steps_in_window": rounding},
                 "roofline": roofline, "cpu_baseline": cb, "e2e": e2e, "gpu_launches": K,
                 "clocks": sampler.summary(), "prefill": prefill, **extra}
         print(json.dumps(line), flush=True)

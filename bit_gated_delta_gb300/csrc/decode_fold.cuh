@@ -325,7 +325,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // an exact integer below 2^24), A = [keys 0..7 | q digits] (M), B = keys (N). (An int8 MMA would take the codes as
   // they are, but on this chip it runs at an eighth of the fp16 rate.)
   {
-    float gacc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};   // two chains of the K steps
+    float gacc[4][4] = {};   // four independent chains of the K steps
     const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;   // the lane's key pair inside its 4-byte load
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
@@ -335,11 +335,12 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       a[2] = i8pair_f16(lds32(krow + g8 * RS + off + 8), sel, false);
       a[1] = g8 < 3 ? i8pair_f16(lds32(krow + (8 + g8) * RS + off), sel, false) : 0u;
       a[3] = g8 < 3 ? i8pair_f16(lds32(krow + (8 + g8) * RS + off + 8), sel, false) : 0u;
-      mma_f16(gacc[ks & 1], a, a[0], a[2]);
+      mma_f16(gacc[ks & 3], a, a[0], a[2]);
     }
-    *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2(gacc[0][0] + gacc[1][0], gacc[0][1] + gacc[1][1]);
-    if (g8 < 3)
-      *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2(gacc[0][2] + gacc[1][2], gacc[0][3] + gacc[1][3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) gacc[0][e] = (gacc[0][e] + gacc[1][e]) + (gacc[2][e] + gacc[3][e]);
+    *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2(gacc[0][0], gacc[0][1]);
+    if (g8 < 3) *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2(gacc[0][2], gacc[0][3]);
   }
   __syncwarp();
 

@@ -145,7 +145,10 @@ pace_status pace_flush(pace_state *state, void *stream);
 
 /* Host-only head ranking ([P1] 무엇과 다른가; [P2] 3. Method & Key Results): E_h = e_h / (1 - a_h^(2 dP))
  * (+inf for a_h >= 1); marks the floor(H*frac) heads with the largest E_h (ties: lower index).
- * e_h, a_h, mask_out are HOST arrays of H entries. Deterministic, no GPU needed. */
+ * e_h, a_h, mask_out are HOST arrays of H entries. Deterministic, no GPU needed.
+ * e_h is the caller's per-head mean over calibration sequences of the per-unit energies that
+ * pace_calib_error_energy writes (e_h = mean over b of e_out[b*H + h]; with the batch split over ranks, sum the
+ * per-rank sums and counts first), and a_h the head's mean decay over its calibration tokens. */
 pace_status pace_assign_heads(const float *e_h, const float *a_h, int H, int dP, float frac,
                               uint8_t *mask_out);
 
