@@ -267,9 +267,6 @@ pace_status pace_decode_step(pace_state *state, const void *q, const void *k, co
   else
     e = pace_launch_decode(state->dev, io, 1, cs);
   if (e != cudaSuccess) return cuda_fail(e, "decode_step launch");
-  // every unit took one token; the step that fills the buffer rounds and empties it
-  if (state->cfg.state_mode != PACE_STATE_BF16 && state->dev.m_hint >= 0)
-    state->dev.m_hint = (state->dev.m_hint + 1) % state->cfg.dP;
   return ok();
 }
 
@@ -282,7 +279,6 @@ pace_status pace_flush(pace_state *state, void *stream) {
   cudaError_t e = state->cfg.state_mode == PACE_STATE_QUANT ? pace_launch_decode_quant(state->dev, io, 0, cs)
                                                             : pace_launch_decode(state->dev, io, 0, cs);
   if (e != cudaSuccess) return cuda_fail(e, "flush launch");
-  state->dev.m_hint = 0;
   return ok();
 }
 
@@ -308,7 +304,6 @@ pace_status pace_prefill_chunk(pace_state *state, int n_tokens, const void *q, c
   PaceIO io{q, k, v, a, beta, o, n_tokens};
   e = pace_prefill_tc_supported(state->dev) ? pace_launch_prefill_tc(state->dev, io, cs) : pace_launch_prefill(state->dev, io, cs);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  state->dev.m_hint = 0;
   return ok();
 }
 
@@ -318,7 +313,6 @@ pace_status pace_quantize_state(pace_state *state, const float *S, void *stream)
   if (!S) return fail(PACE_ERR_INVALID_ARG, "S is NULL");
   cudaError_t e = pace_launch_quantize_state(state->dev, S, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize_state launch");
-  state->dev.m_hint = 0;
   return ok();
 }
 
@@ -373,7 +367,6 @@ pace_status pace_state_import(pace_state *state, const void *src, size_t bytes, 
     return fail(PACE_ERR_INVALID_ARG, "import expects exactly %zu bytes, got %zu", state->lay.total_bytes, bytes);
   cudaError_t e = cudaMemcpyAsync(state->base, src, bytes, cudaMemcpyDefault, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "state import copy");
-  state->dev.m_hint = -1;                          // the imported counts are not known on the host
   return ok();
 }
 

@@ -22,8 +22,6 @@ struct PaceDev {
   float *buf_s;            // [B][H][dP][4]: a, beta, s_k, s_v
   int32_t *m;              // [B][H]
   int32_t *status;         // one word: bit 0 set when a bounded device wait gave up
-  int m_hint;              // the buffer count the host expects every unit to hold (-1: unknown): the decode
-                           // kernels issue those buffered rows before the device count arrives, then check it
   uint32_t probe_ns;       // failure-detection test: > 0 makes the tensor-core prefill wait this long on an
                            // mbarrier that nothing signals, give up and report (pace_test_wait_probe)
   void *S;                 // f32 / bf16 [B][H][D][D]
