@@ -47,6 +47,9 @@ def parse_args(argv=None):
     p.add_argument("--batch", type=int, default=64)
     p.add_argument("--extra", type=int, default=1, help="also time batch 128, the bf16 kernel and prefill")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    p.add_argument("--prefill-only", type=int, default=0, metavar="B",
+                   help="only time two 256-token prefill chunks on one PACE-4 state of B sequences x 32 heads "
+                        "(a small case for profiling the chunk kernel), print one JSON line and exit")
     return p.parse_args(argv)
 
 
@@ -724,6 +727,26 @@ def shared_key_heads(P, torch, peak, B=64, H=32, Hk=16, steps=2000):
             "achieved_gbs": alg / (ms * 1e-3) / 1e9, "frac": alg / (ms * 1e-3) / 1e9 / peak, "rotating_sets": R}
 
 
+def prefill_only(P, torch, B):
+    """Two 256-token chunks of device-drawn inputs through pace_prefill_chunk on one PACE-4 state (B sequences,
+    32 heads, d=128): the chunk kernel on a working set of a few hundred MB, for profiling."""
+    import synth
+    wl = synth.workload("pace4", B=B)
+    st = P.PaceState(P.make_config(wl.H, 128, wl.B, dP=8, group=64), wl.B)
+    o = torch.empty(wl.B, wl.H, 256, 128, dtype=torch.bfloat16, device="cuda")
+    xs = [synth.device_chunk_inputs(wl, 256 * c, 256) for c in range(2)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    us = []
+    for x in xs:
+        ev[0].record()
+        st.prefill_chunk(x["q"], x["k"], x["v"], x["a"], x["beta"], o)
+        ev[1].record()
+        torch.cuda.synchronize()
+        us.append(ev[0].elapsed_time(ev[1]) * 1e3)
+    st.close()
+    print(json.dumps({"prefill_only": {"B": B, "H": wl.H, "chunk_us": us}}), flush=True)
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -741,6 +764,9 @@ def main():
     if not B.up_to_date():
         B.build()
     torch.cuda.set_device(local)
+    if args.prefill_only:
+        prefill_only(P, torch, args.prefill_only)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist

@@ -512,7 +512,9 @@ static cudaError_t launch_bf16buf_t(const PaceDev &d, const PaceIO &io, int has_
 
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
   using namespace pace;
-  if (d.state_mode == PACE_STATE_BF16_BUF)
+  if (d.state_mode == PACE_STATE_BF16_BUF) {
+    if (d.dP <= 8) return pace_launch_decode_bf16buf_fold(d, io, has_token, s);   // periods of up to 8 tokens
     return d.D == 128 ? launch_bf16buf_t<128>(d, io, has_token, s) : launch_bf16buf_t<64>(d, io, has_token, s);
+  }
   return d.D == 128 ? launch_decode_t<128>(d, io, has_token, s) : launch_decode_t<64>(d, io, has_token, s);
 }

@@ -7,7 +7,7 @@
 // The output of the step does not need u. With cq_s = (G_m/G_s) k_s.q and c = diag(beta) (I + L)^-T cq,
 //   o = S_m^T q = G_m S_hat^T q + sum_s cq_s u_s = S_hat^T y + V^T c,   y = G_m q - sum_t c_t G_t k_t,
 // so a step without a rounding reads the packed state once against a single vector y. The per-unit work is an
-// 8 x 8 Gram matrix of the buffered int8 keys (one integer tensor-core MMA per 32 keys, exact), a back
+// 8 x 8 Gram matrix of the buffered int8 keys (fp16 tensor-core MMAs, 16 keys each, exact in fp32), a back
 // substitution across lanes, and y; the state is then contracted with y's three int8 digits (a 24-bit fixed-point
 // image) on the tensor cores, straight from the packed nibbles:
 //   M = state columns (A: the lane's own packed words as fp16 1024 + u, or 1024 + 16u for the second 8 keys of a
@@ -16,6 +16,10 @@
 // contribution of the zero level (computed by the same MMA from a constant operand), so the group fold is one
 // paired multiply-add by the group scale. The rounding step adds the buffered keys as a second N tile, replays
 // each column (four columns per lane) and requantizes the state per key-axis group as in decode_mma.cuh.
+//
+// The same kernel with BITS = 16 serves the buffered bf16 state (int8 decode buffer, bf16 state rounded to bf16
+// once every dP tokens): the prologue (token quantization, Gram, solve, y in fp32) is shared; the state is then read
+// on the CUDA cores, a row of D bf16 values per warp load, against y (and, at a rounding, against the buffered keys).
 #pragma once
 
 #include <type_traits>
@@ -27,24 +31,27 @@ namespace pace {
 constexpr int DF_TOK = 8;   // buffered tokens per unit this kernel handles (dP <= 8)
 
 struct FoldSmem {
-  size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, csx, gram, qk, Lm, tk, ck, total;
+  size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, csx, kf, gram, qk, Lm, tk, ck, total;
 };
 // Per-warp work area. int8 rows use a stride of D + 16 bytes and fp16 digit rows D + 8 halves, so that the
 // fragment loads of the eight rows of a tile fall in distinct banks.
-__host__ __device__ inline FoldSmem fold_smem(int D, int G, int mixed, int zp) {
+__host__ __device__ inline FoldSmem fold_smem(int D, int G, int mixed, int zp, int bf = 0) {
   FoldSmem L;
   size_t off = 0;
   L.krow = carve(off, (size_t)11 * (D + 16));               // key codes of tokens 0..7, then the 3 digits of q
   L.vrow = carve(off, (size_t)DF_TOK * D * (mixed ? 2 : 1)); // value codes (int8) or bf16 values
   L.ydig = carve(off, (size_t)3 * (D + 8) * 2);              // fp16 digit rows of y; packed int4 keys of the
                                                              // mixed buffer while staging
-  L.ssc = carve(off, (size_t)(D / G) * D * 2);               // group scales (bf16), as resident
+  L.ssc = carve(off, bf ? 0 : (size_t)(D / G) * D * 2);      // group scales (bf16), as resident
   L.szp = carve(off, zp ? (size_t)(D / G) * D : 0);          // zero points
   L.po = carve(off, (size_t)D * 4);                          // S_hat^T y per column
   L.pb = carve(off, (size_t)DF_TOK * D * 4);                 // rounding step: P_t then u_t [t][j]
-  L.kbf = carve(off, (size_t)D * 4 * 4);                     // flush B operand: fp16 pairs of int8 keys [i][pair]
+  L.kbf = carve(off, (size_t)D * 4 * 4 * (bf ? 2 : 1));      // flush B operand: fp16 pairs of int8 keys [i][pair];
+                                                             // bf16 state: the keys as fp32 [i][t] (kf)
   // steps without a rounding: the unit's int4 code words are staged over pb, kbf and this spare area
-  L.csx = carve(off, (size_t)D * D / 2 > (L.kbf - L.pb) + (size_t)D * 16 ? (size_t)D * D / 2 - (L.kbf - L.pb) - (size_t)D * 16 : 0);
+  L.csx = carve(off, !bf && (size_t)D * D / 2 > (L.kbf - L.pb) + (size_t)D * 16
+                         ? (size_t)D * D / 2 - (L.kbf - L.pb) - (size_t)D * 16 : 0);
+  L.kf = L.kbf;
   L.gram = carve(off, 64 * 4);                               // k_s.k_t (integers)
   L.qk = carve(off, 3 * 8 * 4);                              // (q digit d).k_t (integers)
   L.Lm = carve(off, 64 * 4);                                 // L[t][s]
@@ -77,6 +84,48 @@ __device__ __forceinline__ void store_io_vec(void *p, size_t idx, const float (&
     else if constexpr (N == 2) *reinterpret_cast<uint32_t *>(h) = bf16x2_bits(x[0], x[1]);
     else h[0] = __float2bfloat16_rn(x[0]);
   }
+}
+
+// N consecutive bf16 values of the bf16 state as floats (N = 1, 2 or 4; 2N-byte aligned).
+template <int N>
+__device__ __forceinline__ void df_load_bf16(const __nv_bfloat16 *p, float (&x)[N]) {
+  if constexpr (N == 4) {
+    const uint2 v = ldg_v2(p);
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+  } else if constexpr (N == 2) {
+    const uint32_t v = ldg_u32(p);
+    x[0] = bf16_lo(v); x[1] = bf16_hi(v);
+  } else {
+    x[0] = __bfloat162float(*p);
+  }
+}
+// Raw N-element bf16 rows (N = 1, 2, 4): load and unpack, so that loads can run ahead of their use.
+template <int N> struct Bf16Raw { uint32_t w[(N + 1) / 2]; };
+template <int N>
+__device__ __forceinline__ Bf16Raw<N> df_ldraw(const __nv_bfloat16 *p) {
+  Bf16Raw<N> r;
+  if constexpr (N == 4) {
+    const uint2 v = ldg_v2(p);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+  } else if constexpr (N == 2) {
+    r.w[0] = ldg_u32(p);
+  } else {
+    r.w[0] = (uint32_t)*reinterpret_cast<const uint16_t *>(p);
+  }
+  return r;
+}
+template <int N>
+__device__ __forceinline__ float df_raw_at(const Bf16Raw<N> &r, int c) {
+  return (c & 1) ? bf16_hi(r.w[c >> 1]) : bf16_lo(r.w[c >> 1]);
+}
+
+// N floats rounded to bf16 (nearest, ties to even) into the bf16 state.
+template <int N>
+__device__ __forceinline__ void df_store_bf16(__nv_bfloat16 *p, const float (&x)[N]) {
+  if constexpr (N == 4) *reinterpret_cast<uint2 *>(p) = make_uint2(bf16x2_bits(x[0], x[1]), bf16x2_bits(x[2], x[3]));
+  else if constexpr (N == 2) *reinterpret_cast<uint32_t *>(p) = bf16x2_bits(x[0], x[1]);
+  else *p = __float2bfloat16_rn(x[0]);
 }
 
 // The lane's packed words of M-tile mt (columns 16 mt .. 16 mt + 15), one 16-byte vector per 64 keys and plane.
@@ -150,14 +199,17 @@ __device__ __forceinline__ void df_sum(const uint32_t (*b)[2], float (&t2)[2]) {
 template <int D, int G, int BITS, int ZP, int MX, int WU>
 __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
                         unsigned char *wsm, int part) {
-  constexpr int CPL = D / 32, NG = D / G, MT = D / 16, NPP = D / 64, PL = BITS / 4, KS = D / 16, KSG = G / 16;
+  // BITS 4 or 8: the packed int4 / int8 state (PACE); BITS 16: the bf16 state of the buffered bf16 mode (row-major,
+  // rounded to bf16 once every dP tokens, the same int8 decode buffer), contracted on the CUDA cores
+  constexpr bool BF = BITS == 16;
+  constexpr int CPL = D / 32, NG = D / G, MT = D / 16, NPP = D / 64, PL = BF ? 1 : BITS / 4, KS = D / 16, KSG = G / 16;
   constexpr int RS = D + 16, YS = D + 8, MTW = MT / WU, CW = D / WU, CPW = CW / 32;
-  constexpr int OFF = 1 << (BITS - 1);
+  constexpr int OFF = BF ? 0 : 1 << (BITS - 1);
   constexpr int NKG = G / 8;
   static_assert(MTW >= 1 && CPW >= 1, "warps per unit");
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int dP = st.dP;
-  const FoldSmem L = fold_smem(D, G, MX, ZP);
+  const FoldSmem L = fold_smem(D, G, MX, ZP, BF);
   int8_t *krow = reinterpret_cast<int8_t *>(wsm + L.krow);
   unsigned char *vrow = wsm + L.vrow;
   __half *ydig = reinterpret_cast<__half *>(wsm + L.ydig);
@@ -172,10 +224,13 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   float4 *tk = reinterpret_cast<float4 *>(wsm + L.tk);
   float *ckf = reinterpret_cast<float *>(wsm + L.ck);
 
-  uint32_t *codes = BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
-                              : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
-  __nv_bfloat16 *scale = st.scale + (size_t)unit * NG * D;
+  uint32_t *codes = BF ? nullptr
+                      : BITS == 4 ? st.codes4 + (size_t)(b * st.H4 + st.head_slot[h]) * (D * D / 8)
+                                  : st.codes8 + (size_t)(b * st.H8 + st.head_slot[h]) * (D * D / 4);
+  __nv_bfloat16 *scale = BF ? nullptr : st.scale + (size_t)unit * NG * D;
   uint8_t *zpt = ZP ? st.zp + (size_t)unit * NG * D : nullptr;
+  __nv_bfloat16 *Sbf = BF ? static_cast<__nv_bfloat16 *>(st.S) + (size_t)unit * D * D : nullptr;   // [i][j]
+  float *kf = reinterpret_cast<float *>(wsm + L.kf);
 
   // ---- loads, in the order the step needs them: the count and the new token; then the buffered rows, their
   // scalars, the scales; the first code tiles once the new token is in
@@ -208,7 +263,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     for (int c = lane; c < m0 * rv / 16; c += 32) cp_async16(vrow + 16 * c, gv + 16 * c);
     if (lane < m0) bs = *reinterpret_cast<const float4 *>(st.buf_s + ((size_t)unit * dP + lane) * 4);
   }
-  {
+  if constexpr (!BF) {
     const char *gs = reinterpret_cast<const char *>(scale);
     for (int c = lane; c < NG * D * 2 / 16; c += 32) cp_async16(reinterpret_cast<char *>(ssc) + 16 * c, gs + 16 * c);
     if (ZP) {
@@ -299,8 +354,10 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 1;" ::: "memory");    // the staging group (the codes may still land)
   } else {
-    df_load_tile<D, PL>(codes, mt0, lane, cwA);
-    if (MTW > 1) df_load_tile<D, PL>(codes, mt0 + 1, lane, cwB);
+    if constexpr (!BF) {
+      df_load_tile<D, PL>(codes, mt0, lane, cwA);
+      if (MTW > 1) df_load_tile<D, PL>(codes, mt0 + 1, lane, cwB);
+    }
     cp_async_wait_all();
   }
   __syncwarp();
@@ -374,7 +431,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       for (int t = 0; t < DF_TOK; ++t) Lm[t * 8 + s] = Lc[t];
     }
     // the flush B operand: kbf[i][p] = fp16 pair (k_{2p,i}, k_{2p+1,i}), zero for tokens >= mt
-    {
+    if constexpr (!BF) {
       const int p = lane & 3, t0 = 2 * p;
       const bool z0 = t0 >= mt, z1 = t0 + 1 >= mt;
 #pragma unroll
@@ -422,6 +479,11 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
         for (int c = 0; c < CPL; ++c) y[c] = fmaf(at, sbyte(kw, c), y[c]);
       }
     }
+    if constexpr (BF) {                            // the bf16 state: y in fp32 (ydig area), read by every lane
+      float *yf = reinterpret_cast<float *>(ydig);
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) yf[CPL * lane + c] = y[c];
+    } else {
     float my = 0.0f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) my = fmaxf(my, fabsf(y[c]));
@@ -462,13 +524,14 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       yb[ks][0] = g8 < 3 ? lds32(ydig + g8 * YS + 16 * ks + 2 * tq) : 0u;
       yb[ks][1] = g8 < 3 ? lds32(ydig + g8 * YS + 16 * ks + 8 + 2 * tq) : 0u;
     }
+    }
   } else {
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) yb[ks][0] = yb[ks][1] = 0u;
   }
   // B fragments of the buffered keys (rounding step): token g8's keys as fp16, second halves / 16
   uint32_t kb[KS][2];
-  if (do_flush) {
+  if (!BF && do_flush) {
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const uint32_t x0 = g8 < mt ? lds32(krow + g8 * RS + 16 * ks + 4 * (tq >> 1)) : 0u;
@@ -483,7 +546,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // points and int8 planes, the plain sums T2
   float offy[NG][PL][2] = {}, t2y[NG][2] = {}, offk[NG][PL][2] = {}, t2k[NG][2] = {};
 #pragma unroll
-  for (int g = 0; g < NG; ++g) {
+  for (int g = 0; g < (BF ? 0 : NG); ++g) {
 #pragma unroll
     for (int pl = 0; pl < PL; ++pl) {
       // int4 symmetric: every code at 8 -> -(T1 + 8 T2); int8 symmetric: low plane 0, high plane 8; zero point: 0
@@ -501,7 +564,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   if (smem_codes) {
     cp_async_wait_all();
     __syncwarp();
-  } else if (MTW > 2 && lane < PL) {
+  } else if (!BF && MTW > 2 && lane < PL) {
     constexpr uint32_t TW = NPP * 128;             // words of one M-tile in a plane
     prefetch_l2(codes + lane * (D * D / 8) + (mt0 + 2) * TW, (MTW - 2) * TW * 4);
   }
@@ -619,8 +682,79 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       }
     }
   };
-  if (do_flush) dots(std::true_type{});
-  else dots(std::false_type{});
+  if constexpr (BF) {
+    // ---- the bf16 state on the CUDA cores: lane = CPW consecutive columns (8-, 4- or 2-byte loads, coalesced
+    // across the warp), rows streamed through a window of loads in flight (32 rows on a step without a rounding, 8
+    // at a rounding, where the registers also hold the eight key dots); S_hat^T y into po, and at a rounding
+    // S_hat^T k_t (key codes) into pb
+    const float *yf = reinterpret_cast<const float *>(ydig);
+    const int jb = part * CW + CPW * lane;
+    __syncwarp();                                  // y, written by every lane, is read by every lane
+    if (do_flush) {                                // the keys as fp32 [i][t] (zero for t >= mt)
+      for (int idx = lane; idx < D * DF_TOK; idx += 32) {
+        const int i = idx >> 3, t = idx & 7;
+        kf[idx] = t < mt ? (float)krow[t * RS + i] : 0.0f;
+      }
+      __syncwarp();
+    }
+    float acc[CPW] = {};
+    if (!do_flush) {
+      // rows streamed through a window of PD loads in flight (row r + PD requested as row r is used)
+      constexpr int PD = 32;
+      Bf16Raw<CPW> win[PD];
+#pragma unroll
+      for (int r = 0; r < PD; ++r) win[r] = df_ldraw<CPW>(Sbf + (size_t)r * D + jb);
+#pragma unroll 1
+      for (int i0 = 0; i0 < D; i0 += PD) {
+#pragma unroll
+        for (int rr = 0; rr < PD; ++rr) {
+          const Bf16Raw<CPW> v = win[rr];
+          if (i0 + PD < D) win[rr] = df_ldraw<CPW>(Sbf + (size_t)(i0 + PD + rr) * D + jb);
+          const float yi = yf[i0 + rr];
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) acc[c] = fmaf(yi, df_raw_at<CPW>(v, c), acc[c]);
+        }
+      }
+    } else {
+      float pk[DF_TOK][CPW] = {};
+      constexpr int PD = 8;
+      Bf16Raw<CPW> win[PD];
+#pragma unroll
+      for (int r = 0; r < PD; ++r) win[r] = df_ldraw<CPW>(Sbf + (size_t)r * D + jb);
+#pragma unroll 1
+      for (int i0 = 0; i0 < D; i0 += PD) {
+#pragma unroll
+        for (int rr = 0; rr < PD; ++rr) {
+          const Bf16Raw<CPW> v = win[rr];
+          if (i0 + PD < D) win[rr] = df_ldraw<CPW>(Sbf + (size_t)(i0 + PD + rr) * D + jb);
+          const float yi = has_token ? yf[i0 + rr] : 0.0f;
+          const float4 ka = *reinterpret_cast<const float4 *>(kf + (i0 + rr) * DF_TOK);
+          const float4 kb4 = *reinterpret_cast<const float4 *>(kf + (i0 + rr) * DF_TOK + 4);
+          const float kr[8] = {ka.x, ka.y, ka.z, ka.w, kb4.x, kb4.y, kb4.z, kb4.w};
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) {
+            const float x = df_raw_at<CPW>(v, c);
+            acc[c] = fmaf(yi, x, acc[c]);
+#pragma unroll
+            for (int t = 0; t < DF_TOK; ++t) pk[t][c] = fmaf(kr[t], x, pk[t][c]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < DF_TOK; ++t)
+        if (t < mt) {
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) pb[t * D + jb + c] = pk[t][c];
+        }
+    }
+    if (has_token) {
+#pragma unroll
+      for (int c = 0; c < CPW; ++c) po[jb + c] = acc[c];
+    }
+  } else {
+    if (do_flush) dots(std::true_type{});
+    else dots(std::false_type{});
+  }
   __syncwarp();
 
   // ---- output (lane: CPW consecutive columns of the warp's range): o = S_hat^T y + V^T c
@@ -679,6 +813,38 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     }
     __syncwarp();
 
+    if constexpr (BF) {
+      // ---- rounding of the bf16 state: S_new[i][j] = bf16(G_m S[i][j] + sum_s k_si (rho_s u_sj)), the lane's columns
+      float w[DF_TOK][CPW];
+#pragma unroll
+      for (int t = 0; t < DF_TOK; ++t)
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) w[t][c] = t < mt ? ckf[t] * u[t][c] : 0.0f;
+      constexpr int PD = 8;
+      Bf16Raw<CPW> win[PD];
+#pragma unroll
+      for (int r = 0; r < PD; ++r) win[r] = df_ldraw<CPW>(Sbf + (size_t)r * D + jc);
+#pragma unroll 1
+      for (int i0 = 0; i0 < D; i0 += PD) {
+#pragma unroll
+        for (int rr = 0; rr < PD; ++rr) {
+          const Bf16Raw<CPW> v = win[rr];
+          if (i0 + PD < D) win[rr] = df_ldraw<CPW>(Sbf + (size_t)(i0 + PD + rr) * D + jc);
+          const float4 ka = *reinterpret_cast<const float4 *>(kf + (i0 + rr) * DF_TOK);
+          const float4 kb4 = *reinterpret_cast<const float4 *>(kf + (i0 + rr) * DF_TOK + 4);
+          const float kr[8] = {ka.x, ka.y, ka.z, ka.w, kb4.x, kb4.y, kb4.z, kb4.w};
+          float x[CPW];
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) {
+            float vv = Gm * df_raw_at<CPW>(v, c);
+#pragma unroll
+            for (int t = 0; t < DF_TOK; ++t) vv = fmaf(kr[t], w[t][c], vv);
+            x[c] = vv;
+          }
+          df_store_bf16<CPW>(Sbf + (size_t)(i0 + rr) * D + jc, x);
+        }
+      }
+    } else {
     // ---- rounding of the warp's M-tiles: S_new^T[j][i] = sum_s rho_s u_sj k_si + G_m s_gj (u_ij - z_gj)
     const int dpp = 8;
     uint32_t cwn[PL][NPP][4];                      // the next tile's words, requested one tile ahead
@@ -834,6 +1000,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
               make_uint4(cw[pl][pp][0], cw[pl][pp][1], cw[pl][pp][2], cw[pl][pp][3]);
     }
   }
+  }
   // every warp of the unit has read the count before it moves on
   if (WU > 1) __syncthreads(); else __syncwarp();
   if (threadIdx.x == 0) st.m[unit] = do_flush ? 0 : mt;
@@ -841,23 +1008,23 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 
 // One unit per block of WU warps; one launch per code pool (int4 heads, int8 heads).
 template <int D, int G, int BITS, int ZP, int MX, int WU>
-__global__ void __launch_bounds__(WU * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : 12) / WU)
+__global__ void __launch_bounds__(WU * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : BITS == 16 ? 16 : 12) / WU)
     decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_enter();
   const int warp = threadIdx.x >> 5;
-  const int HP = BITS == 4 ? st.H4 : st.H8;
+  const int HP = BITS == 8 ? st.H8 : st.H4;   // (the bf16 state: every head, in the first pool)
   const int w = blockIdx.x;
   if (w >= st.B * HP) return;
   const int b = w / HP, slot = w - b * HP;
-  const int h = st.pool_head[(BITS == 4 ? 0 : st.H4) + slot];
-  const FoldSmem L = fold_smem(D, G, MX, ZP);
+  const int h = st.pool_head[(BITS == 8 ? st.H4 : 0) + slot];
+  const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16);
   df_unit<D, G, BITS, ZP, MX, WU>(st, io, b, h, b * st.H + h, has_token, smem + (size_t)warp * L.total, warp);
 }
 
 template <int D, int G, int BITS, int ZP, int MX, int WU>
 static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, long units) {
-  const FoldSmem L = fold_smem(D, G, MX, ZP);
+  const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16);
   const size_t smem = (size_t)WU * L.total;
   cudaError_t e = smem_opt_in<decode_fold_kernel<D, G, BITS, ZP, MX, WU>>(smem);
   if (e != cudaSuccess) return e;
@@ -870,7 +1037,7 @@ static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_tok
 // slots, two (four) warps share each unit and split its M-tiles, which shortens the per-unit chain.
 template <int D, int G, int BITS, int ZP, int MX>
 static cudaError_t launch_fold_pool(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  const long units = (long)d.B * (BITS == 4 ? d.H4 : d.H8);
+  const long units = (long)d.B * (BITS == 8 ? d.H8 : d.H4);
   if (units == 0) return cudaSuccess;
   const long slots = (long)device_sm_count() * 16;
   if constexpr (D >= 128) {                      // (at least 32 columns per warp)
@@ -901,6 +1068,11 @@ cudaError_t launch_fold_zm(const PaceDev &d, const PaceIO &io, int has_token, cu
     }
   }
   return e;
+}
+// The buffered bf16 state (PACE_STATE_BF16_BUF: int8 buffer, bf16 state rounded once every dP tokens).
+inline cudaError_t launch_fold_bf16buf(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  return d.D == 128 ? launch_fold_pool<128, 64, 16, 0, 0>(d, io, has_token, s)
+                    : launch_fold_pool<64, 64, 16, 0, 0>(d, io, has_token, s);
 }
 extern template cudaError_t launch_fold_zm<0, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
 extern template cudaError_t launch_fold_zm<0, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);

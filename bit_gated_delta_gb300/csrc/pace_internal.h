@@ -51,6 +51,8 @@ struct PaceIO {
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
+// Buffered bf16 state with dP <= 8 on the folded-readout kernel (decode_fold.cuh).
+cudaError_t pace_launch_decode_bf16buf_fold(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 // Tensor-core chunk prefill (d_k = d_v = 128, bf16 I/O); pace_prefill_tc_supported says whether it applies.
 bool pace_prefill_tc_supported(const PaceDev &d);
