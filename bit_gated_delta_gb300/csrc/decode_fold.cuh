@@ -1047,32 +1047,32 @@ static cudaError_t launch_fold_pool(const PaceDev &d, const PaceIO &io, int has_
   return launch_fold_w<D, G, BITS, ZP, MX, 1>(d, io, has_token, s, units);
 }
 
-template <int ZP, int MX>
-cudaError_t launch_fold_zm(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  cudaError_t e;
-  if (d.D == 128) {
-    if (d.G == 64) {
-      e = launch_fold_pool<128, 64, 4, ZP, MX>(d, io, has_token, s);
-      if (e == cudaSuccess) e = launch_fold_pool<128, 64, 8, ZP, MX>(d, io, has_token, s);
-    } else {
-      e = launch_fold_pool<128, 32, 4, ZP, MX>(d, io, has_token, s);
-      if (e == cudaSuccess) e = launch_fold_pool<128, 32, 8, ZP, MX>(d, io, has_token, s);
-    }
-  } else {
-    if (d.G == 64) {
-      e = launch_fold_pool<64, 64, 4, ZP, MX>(d, io, has_token, s);
-      if (e == cudaSuccess) e = launch_fold_pool<64, 64, 8, ZP, MX>(d, io, has_token, s);
-    } else {
-      e = launch_fold_pool<64, 32, 4, ZP, MX>(d, io, has_token, s);
-      if (e == cudaSuccess) e = launch_fold_pool<64, 32, 8, ZP, MX>(d, io, has_token, s);
-    }
+// The int4 and int8 pools touch disjoint units: with both present, the int8 pool runs on the state's side stream,
+// forked from s after everything already queued there and joined back before anything queued later, so the two
+// launches share the SMs (each pool alone leaves part of a wave idle).
+template <int D, int G, int ZP, int MX>
+static cudaError_t launch_fold_pools(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  if (!d.side || d.H4 == 0 || d.H8 == 0) {
+    cudaError_t e = launch_fold_pool<D, G, 4, ZP, MX>(d, io, has_token, s);
+    if (e == cudaSuccess) e = launch_fold_pool<D, G, 8, ZP, MX>(d, io, has_token, s);
+    return e;
   }
+  cudaError_t e = cudaEventRecord(d.ev_fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d.side, d.ev_fork, 0);
+  if (e == cudaSuccess) e = launch_fold_pool<D, G, 8, ZP, MX>(d, io, has_token, d.side);
+  if (e == cudaSuccess) e = cudaEventRecord(d.ev_join, d.side);
+  if (e == cudaSuccess) e = launch_fold_pool<D, G, 4, ZP, MX>(d, io, has_token, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, d.ev_join, 0);
   return e;
 }
-// The buffered bf16 state (PACE_STATE_BF16_BUF: int8 buffer, bf16 state rounded once every dP tokens).
-inline cudaError_t launch_fold_bf16buf(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  return d.D == 128 ? launch_fold_pool<128, 64, 16, 0, 0>(d, io, has_token, s)
-                    : launch_fold_pool<64, 64, 16, 0, 0>(d, io, has_token, s);
+
+template <int ZP, int MX>
+cudaError_t launch_fold_zm(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
+  if (d.D == 128)
+    return d.G == 64 ? launch_fold_pools<128, 64, ZP, MX>(d, io, has_token, s)
+                     : launch_fold_pools<128, 32, ZP, MX>(d, io, has_token, s);
+  return d.G == 64 ? launch_fold_pools<64, 64, ZP, MX>(d, io, has_token, s)
+                   : launch_fold_pools<64, 32, ZP, MX>(d, io, has_token, s);
 }
 extern template cudaError_t launch_fold_zm<0, 0>(const PaceDev &, const PaceIO &, int, cudaStream_t);
 extern template cudaError_t launch_fold_zm<0, 1>(const PaceDev &, const PaceIO &, int, cudaStream_t);

@@ -3,5 +3,7 @@
 #include "decode_fold.cuh"
 
 cudaError_t pace_launch_decode_bf16buf_fold(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s) {
-  return pace::launch_fold_bf16buf(d, io, has_token, s);
+  using namespace pace;
+  return d.D == 128 ? launch_fold_pool<128, 64, 16, 0, 0>(d, io, has_token, s)
+                    : launch_fold_pool<64, 64, 16, 0, 0>(d, io, has_token, s);
 }

@@ -229,11 +229,27 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
     delete s;
     return cuda_fail(e, "zeroing the state");
   }
+  if (cfg->state_mode == PACE_STATE_QUANT && L.H4 > 0 && L.H8 > 0) {
+    e = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      pace_state_free(s);
+      return cuda_fail(e, "creating the int8-pool stream");
+    }
+  }
   *out = s;
   return ok();
 }
 
-void pace_state_free(pace_state *state) { delete state; }
+void pace_state_free(pace_state *state) {
+  if (!state) return;
+  const PaceDev &d = state->dev;
+  if (d.ev_join) cudaEventDestroy(d.ev_join);
+  if (d.ev_fork) cudaEventDestroy(d.ev_fork);
+  if (d.side) cudaStreamDestroy(d.side);
+  delete state;
+}
 
 pace_status pace_state_get_layout(const pace_state *state, pace_layout *out) {
   pace_status st = check_state(state);

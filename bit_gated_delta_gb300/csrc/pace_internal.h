@@ -25,6 +25,10 @@ struct PaceDev {
   uint32_t probe_ns;       // failure-detection test: > 0 makes the tensor-core prefill wait this long on an
                            // mbarrier that nothing signals, give up and report (pace_test_wait_probe)
   void *S;                 // f32 / bf16 [B][H][D][D]
+  // host-side: with int4 and int8 heads both present, the int8-head pool of a decode step runs on this state's own
+  // stream, forked from the caller's stream and joined back into it (null otherwise)
+  cudaStream_t side;
+  cudaEvent_t ev_fork, ev_join;
   uint8_t head_is_int8[PACE_MAX_HEADS];
   int16_t head_slot[PACE_MAX_HEADS];
   int16_t pool_head[PACE_MAX_HEADS];   // heads of the int4 pool in slot order, then those of the int8 pool
