@@ -114,10 +114,14 @@ pace_status pace_state_bytes(const pace_config *cfg, const uint8_t *head_is_int8
 
 /* Bind a caller-owned device region of `bytes` (>= pace_state_bytes, 256-byte aligned) to a new state
  * handle for `batch` (1..max_batch) sequences, and enqueue its zeroing on `stream` (zero state,
- * empty buffers). The handle is host memory; release it with pace_state_free. */
+ * empty buffers). The handle is host memory; release it with pace_state_free. A quantized state with
+ * both int4 and int8 heads also gets its own non-blocking CUDA stream and two events (created on the
+ * current device): decode steps run the int8-head pool there, forked from and joined back into the
+ * caller's stream, so that the two pools share the SMs; every call stays ordered on its `stream`. */
 pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8, void *device_mem,
                              size_t bytes, int batch, void *stream, pace_state **out);
-/* Frees the host handle only; the device region stays the caller's. NULL is accepted. */
+/* Frees the host handle (and the stream and events of a state with both int4 and int8 heads; work
+ * already queued completes); the device region stays the caller's. NULL is accepted. */
 void pace_state_free(pace_state *state);
 pace_status pace_state_get_layout(const pace_state *state, pace_layout *out);
 
