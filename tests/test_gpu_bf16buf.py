@@ -78,3 +78,20 @@ def test_small_head_dim_fp32_io(P):
         assert ok, f"step {step}: {msg}"
         if (step + 1) % wl.dP == 0:
             check_state_and_sync(run, f"step {step}")
+
+
+@pytest.mark.parametrize("B", [24, 64])
+def test_launch_shapes_at_32_heads(P, B):
+    """d = 128, 32 heads: B = 24 runs two warps per unit, B = 64 (the bench configuration) one warp per unit and
+    16 units per SM; 8 sampled units against the oracle over two periods."""
+    wl = synth.workload("pace4", B=B)
+    sample = [(b, h) for b, h in ((0, 0), (1, 31), (B // 2, 7), (B - 1, 16), (3, 3), (B - 2, 30), (5, 12), (B - 3, 1))]
+    run = PairRun(wl, state_mode=P.PACE_STATE_BF16_BUF, sample=sample)
+    run.prefill(256)
+    check_state_and_sync(run, "prefill")
+    for step in range(2 * wl.dP):
+        g, r = run.decode()
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"B={B} step {step}: {msg}"
+        if (step + 1) % wl.dP == 0:
+            check_state_and_sync(run, f"B={B} step {step}")

@@ -202,3 +202,40 @@ def test_layer_stack_inputs(P):
             if (step + 1) % wl.dP == 0:
                 frac, dmax = run.check_round_and_sync()
                 assert frac >= 0.999 and dmax <= 1
+
+
+def test_two_pools_replayed_from_a_cuda_graph(P):
+    """A state with int4 and int8 heads runs its int8 pool on the state's own stream, forked from and joined
+    back into the caller's stream. Captured in a CUDA graph and replayed step after step, every output and
+    every rounding still matches the oracle (the fork and join become graph edges)."""
+    import torch
+    wl = synth.workload("pace48", B=4, H=8)
+    mask = np.zeros(wl.H, np.uint8)
+    mask[[1, 6]] = 1
+    run = PairRun(wl, mask=mask)
+    run.prefill(256)
+    run.check_round_and_sync("prefill")
+    static = [torch.zeros(wl.B, wl.H, wl.d_k, device="cuda", dtype=torch.bfloat16) for _ in range(2)]
+    static += [torch.zeros(wl.B, wl.H, wl.d_v, device="cuda", dtype=torch.bfloat16)]
+    static += [torch.zeros(wl.B, wl.H, device="cuda", dtype=torch.float32) for _ in range(2)]
+    static += [torch.zeros(wl.B, wl.H, wl.d_v, device="cuda", dtype=torch.bfloat16)]
+    run.decode()                                   # one direct step first: the kernels' attributes are set
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):                  # records the step without running it
+        run.state.decode_step(*static)
+    torch.cuda.synchronize()
+    assert (read_blob(run.state).m() == 1).all(), "capturing must not run the step"
+
+    def replay(q, k, v, a, beta, o):
+        for dst, src in zip(static[:5], (q, k, v, a, beta)):
+            dst.copy_(src)
+        graph.replay()
+        o.copy_(static[5])
+
+    for step in range(2, 2 * wl.dP + 2):          # step 1 was the direct one
+        g, r = run.decode(gpu_call=replay)
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"step {step}: {msg}"
+        if step % wl.dP == 0:
+            run.check_round_and_sync(f"step {step}")
+            assert (read_blob(run.state).m() == 0).all()
