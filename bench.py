@@ -279,6 +279,8 @@ def time_steps(torch, setup, K, W, sampler=None):
     """Run W warm-up steps, then exactly K timed steps; returns ms per step (CUDA events)."""
     G = setup.R * setup.wl.dP if setup.cfg.state_mode != 2 else setup.R
     G = min(G, max(1, K))
+    nvtx = torch.cuda.nvtx
+    nvtx.range_push(f"decode warm-up B={setup.wl.B} H={setup.wl.H}")
     g = setup.graph(G)
     for _ in range((W + G - 1) // G):
         g.replay()
@@ -286,11 +288,13 @@ def time_steps(torch, setup, K, W, sampler=None):
     tail = K % G
     gt = setup.graph(tail) if tail else None
     torch.cuda.synchronize()
+    nvtx.range_pop()
     setup.window_roundings = setup.rounding_steps(K)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ctx = sampler if sampler is not None else _Null()
     with ctx:
         torch.cuda.synchronize()
+        nvtx.range_push(f"decode timed {K} steps B={setup.wl.B} H={setup.wl.H}")
         ev0.record()
         for _ in range(K // G):
             g.replay()
@@ -298,6 +302,7 @@ def time_steps(torch, setup, K, W, sampler=None):
             gt.replay()
         ev1.record()
         torch.cuda.synchronize()
+        nvtx.range_pop()
     return ev0.elapsed_time(ev1) / K
 
 

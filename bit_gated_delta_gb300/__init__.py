@@ -10,19 +10,21 @@ import ctypes as C
 
 import numpy as np
 
-from ._lib import (PACE_BUF_FP32, PACE_BUF_INT8, PACE_BUF_MIXED, PACE_ERR_TIMEOUT, PACE_IO_BF16, PACE_IO_F32, PACE_MAX_DP,
-                   PACE_MAX_HEADS, PACE_STATE_BF16, PACE_STATE_BF16_BUF, PACE_STATE_FP32, PACE_STATE_QUANT, PaceError, check, lib,
-                   pace_config, pace_layout)
+from ._lib import (PACE_BUF_FP32, PACE_BUF_INT8, PACE_BUF_MIXED, PACE_ERR_STATE, PACE_ERR_TIMEOUT, PACE_IO_BF16,
+                   PACE_IO_F32, PACE_MAX_DP, PACE_MAX_HEADS, PACE_STATE_BF16, PACE_STATE_BF16_BUF, PACE_STATE_FP32,
+                   PACE_STATE_QUANT, PACE_GUARD_BYTES, PACE_VALIDATE_N, PaceError, check, lib, pace_config, pace_layout)
 
 __all__ = [
     "pace_config", "make_config", "pace_state_bytes", "pace_state_alloc", "pace_state_free",
     "pace_state_get_layout", "pace_prefill_chunk", "pace_decode_step", "pace_flush", "pace_assign_heads",
     "pace_quantize_state", "pace_dequantize_state", "pace_calib_error_energy", "pace_calib_error_energy_axis",
     "pace_state_export",
-    "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_test_wait_probe", "pace_last_error", "pace_version",
-    "PaceState", "PaceError", "PACE_ERR_TIMEOUT",
+    "pace_state_import", "pace_resident_bits", "pace_get_status", "pace_test_wait_probe", "pace_validate_state",
+    "pace_last_error", "pace_version", "VALIDATE_FIELDS",
+    "PaceState", "PaceError", "PACE_ERR_TIMEOUT", "PACE_ERR_STATE",
     "PACE_STATE_QUANT", "PACE_STATE_FP32", "PACE_STATE_BF16", "PACE_STATE_BF16_BUF", "PACE_BUF_INT8", "PACE_BUF_MIXED",
-    "PACE_BUF_FP32", "PACE_IO_BF16", "PACE_IO_F32", "PACE_MAX_HEADS", "PACE_MAX_DP",
+    "PACE_BUF_FP32", "PACE_IO_BF16", "PACE_IO_F32", "PACE_MAX_HEADS", "PACE_MAX_DP", "PACE_GUARD_BYTES",
+    "PACE_VALIDATE_N",
 ]
 
 
@@ -150,6 +152,20 @@ def pace_test_wait_probe(handle, ns: int) -> None:
     check(lib().pace_test_wait_probe(handle, int(ns)))
 
 
+VALIDATE_FIELDS = ("bad_counters", "bad_scales_or_values", "bad_zero_points", "unused_level_codes",
+                   "bad_buffer_values", "changed_guard_bytes")
+
+
+def pace_validate_state(handle, stream=None) -> dict:
+    """Debug check of a state (synchronises the stream): the counts of pace_validate_state by name. A non-zero
+    count is reported in the dict, not raised; other errors raise PaceError."""
+    out = (C.c_int64 * PACE_VALIDATE_N)()
+    st = lib().pace_validate_state(handle, out, _stream(stream))
+    if st != PACE_ERR_STATE:
+        check(st)
+    return dict(zip(VALIDATE_FIELDS, (int(x) for x in out)))
+
+
 def pace_resident_bits(cfg: pace_config, head_is_int8=None, literal_formula: bool = True) -> float:
     keep, mp = _mask(head_is_int8)
     return float(lib().pace_resident_bits(C.byref(cfg), mp, int(literal_formula)))
@@ -182,6 +198,9 @@ class PaceState:
 
     def flush(self, stream=None):
         pace_flush(self.handle, stream)
+
+    def validate(self, stream=None) -> dict:
+        return pace_validate_state(self.handle, stream)
 
     def close(self):
         if getattr(self, "handle", None):

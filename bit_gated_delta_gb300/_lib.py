@@ -16,6 +16,8 @@ PACE_BUF_INT8, PACE_BUF_MIXED, PACE_BUF_FP32 = 0, 1, 2
 PACE_IO_BF16, PACE_IO_F32 = 0, 1
 PACE_MAX_HEADS = 256
 PACE_MAX_DP = 32
+PACE_VALIDATE_N = 6
+PACE_GUARD_BYTES = 256
 _STATUS_NAMES = {0: "PACE_OK", 1: "PACE_ERR_INVALID_ARG", 2: "PACE_ERR_UNSUPPORTED", 3: "PACE_ERR_STATE",
                  4: "PACE_ERR_CUDA", 5: "PACE_ERR_TIMEOUT"}
 
@@ -64,6 +66,7 @@ _SIGS = {
     "pace_resident_bits": (_D, [C.POINTER(pace_config), _PU8, _I]),
     "pace_get_status": (_I, [_VP, _I, C.POINTER(C.c_int), _VP]),
     "pace_test_wait_probe": (_I, [_VP, C.c_uint32]),
+    "pace_validate_state": (_I, [_VP, C.POINTER(C.c_int64), _VP]),
 }
 
 

@@ -80,7 +80,8 @@ pace_status validate_config(const pace_config *c, const uint8_t *mask) {
 }
 
 // Offsets of every resident array for `batch` sequences.
-pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
+pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch, size_t *guard = nullptr,
+                        int *n_guards = nullptr) {
   pace_layout L;
   memset(&L, 0, sizeof L);
   const size_t none = (size_t)-1;
@@ -97,9 +98,13 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
   L.H4 = h4;
   L.H8 = h8;
   size_t off = 0;
-  auto take = [&](size_t &field, size_t bytes) {
+  int ng = 0;
+  auto take = [&](size_t &field, size_t bytes) {   // the array, then its guard region
     field = off;
     off = align256(off + bytes);
+    if (guard && ng < PACE_MAX_GUARDS) guard[ng] = off;
+    ++ng;
+    off += PACE_GUARD_BYTES;
   };
   if (c->state_mode == PACE_STATE_QUANT) {
     take(L.codes4, B * h4 * (D / 8) * D * 4);
@@ -128,8 +133,9 @@ pace_layout make_layout(const pace_config *c, const uint8_t *mask, int batch) {
     take(L.S, B * H * D * D * 2);
   }
   take(L.m, B * H * 4);
-  take(L.status, 4);
+  take(L.status, 64 * 4);
   L.total_bytes = off;
+  if (n_guards) *n_guards = ng;
   return L;
 }
 
@@ -172,7 +178,9 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
   if (!device_mem) return fail(PACE_ERR_INVALID_ARG, "device_mem is NULL");
   if (reinterpret_cast<uintptr_t>(device_mem) % 256)
     return fail(PACE_ERR_INVALID_ARG, "device_mem must be 256-byte aligned");
-  const pace_layout L = make_layout(cfg, head_is_int8, batch);
+  size_t guard[PACE_MAX_GUARDS];
+  int n_guards = 0;
+  const pace_layout L = make_layout(cfg, head_is_int8, batch, guard, &n_guards);
   if (bytes < L.total_bytes)
     return fail(PACE_ERR_INVALID_ARG, "device region of %zu bytes is smaller than the %zu the state needs", bytes,
                 L.total_bytes);
@@ -183,6 +191,8 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
   s->lay = L;
   s->base = static_cast<char *>(device_mem);
   s->bytes = bytes;
+  s->n_guards = n_guards;
+  for (int g = 0; g < n_guards; ++g) s->guard[g] = guard[g];
   PaceDev &d = s->dev;
   memset(&d, 0, sizeof d);
   d.B = batch;
@@ -225,6 +235,7 @@ pace_status pace_state_alloc(const pace_config *cfg, const uint8_t *head_is_int8
     if (e == cudaSuccess && L.H8)
       e = cudaMemset2DAsync(reinterpret_cast<char *>(d.codes8) + plane, 2 * plane, 0x88, plane, (size_t)batch * L.H8, cs);
   }
+  for (int g = 0; g < n_guards && e == cudaSuccess; ++g) e = cudaMemsetAsync(s->base + guard[g], 0xA5, PACE_GUARD_BYTES, cs);
   if (e != cudaSuccess) {
     delete s;
     return cuda_fail(e, "zeroing the state");
@@ -408,6 +419,31 @@ pace_status pace_get_status(const pace_state *state, int clear, int *status_out,
   return ok();
 }
 
+pace_status pace_validate_state(const pace_state *state, int64_t *counts_out, void *stream) {
+  pace_status st = check_state(state);
+  if (st != PACE_OK) return st;
+  if (!counts_out) return fail(PACE_ERR_INVALID_ARG, "counts_out is NULL");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // the counts live in the status array (words 16..27) of the caller's region: the library allocates nothing
+  unsigned long long *dev = reinterpret_cast<unsigned long long *>(state->base + state->lay.status + 64);
+  unsigned long long host[PACE_VALIDATE_N] = {};
+  cudaError_t e = cudaMemsetAsync(dev, 0, sizeof host, cs);
+  if (e == cudaSuccess) e = pace_launch_validate(state->dev, state->base, state->guard, state->n_guards, dev, cs);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host, dev, sizeof host, cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e, "validating the state");
+  unsigned long long any = 0;
+  for (int k = 0; k < PACE_VALIDATE_N; ++k) {
+    counts_out[k] = (int64_t)host[k];
+    any |= host[k];
+  }
+  if (any)
+    return fail(PACE_ERR_STATE, "state check: %llu counters, %llu scales/values, %llu zero points, %llu unused-level "
+                "codes, %llu buffer values, %llu guard bytes out of range", host[0], host[1], host[2], host[3], host[4],
+                host[5]);
+  return ok();
+}
+
 pace_status pace_assign_heads(const float *e_h, const float *a_h, int H, int dP, float frac, uint8_t *mask_out) {
   if (!e_h || !a_h || !mask_out) return fail(PACE_ERR_INVALID_ARG, "assign_heads: NULL array");
   if (H < 1 || H > PACE_MAX_HEADS) return fail(PACE_ERR_INVALID_ARG, "H %d outside 1..%d", H, PACE_MAX_HEADS);
@@ -434,8 +470,9 @@ double pace_resident_bits(const pace_config *cfg, const uint8_t *head_is_int8, i
   const double D = cfg->d_k, H = cfg->n_heads;
   const double values = (double)cfg->max_batch * H * D * D;
   if (!literal_formula) {
-    const pace_layout L = make_layout(cfg, head_is_int8, cfg->max_batch);
-    return 8.0 * (double)L.total_bytes / values;
+    int ng = 0;
+    const pace_layout L = make_layout(cfg, head_is_int8, cfg->max_batch, nullptr, &ng);
+    return 8.0 * (double)(L.total_bytes - (size_t)ng * PACE_GUARD_BYTES) / values;   // (guards are not state)
   }
   if (cfg->state_mode == PACE_STATE_FP32) return 32.0 + 0.0;
   if (cfg->state_mode == PACE_STATE_BF16) return 16.0;

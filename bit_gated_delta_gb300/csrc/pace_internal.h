@@ -34,6 +34,8 @@ struct PaceDev {
   int16_t pool_head[PACE_MAX_HEADS];   // heads of the int4 pool in slot order, then those of the int8 pool
 };
 
+constexpr int PACE_MAX_GUARDS = 16;
+
 struct pace_state {
   pace_config cfg;
   int batch;
@@ -41,6 +43,8 @@ struct pace_state {
   char *base;
   size_t bytes;
   PaceDev dev;
+  int n_guards;                   // guard regions (PACE_GUARD_BYTES each, 0xA5) after the arrays of the region
+  size_t guard[PACE_MAX_GUARDS];  // their offsets
 };
 
 // Per-call pointers of one decode step / flush / prefill chunk.
@@ -62,6 +66,9 @@ cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t
 bool pace_prefill_tc_supported(const PaceDev &d);
 cudaError_t pace_launch_prefill_tc(const PaceDev &d, const PaceIO &io, cudaStream_t s);
 cudaError_t pace_launch_quantize_state(const PaceDev &d, const float *S, cudaStream_t s);
+// Counting kernel of pace_validate_state: adds the PACE_VALIDATE_N counts into counts (device, zeroed by the caller).
+cudaError_t pace_launch_validate(const PaceDev &d, const char *base, const size_t *guard, int n_guards,
+                                 unsigned long long *counts, cudaStream_t s);
 cudaError_t pace_launch_dequantize_state(const PaceDev &d, float *S, cudaStream_t s);
 cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_point, int axis, float *e_out,
                               cudaStream_t s);

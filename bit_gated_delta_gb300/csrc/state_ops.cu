@@ -3,6 +3,7 @@
 //   dequantize_state: resident format -> fp32 S
 //   calib:            e[b,h] = || Q(S) - S ||_F^2 of an fp32 state, the error energy of one rounding that
 //                     the ranking E_h = e_h / (1 - a_h^(2 dP)) uses ([P1] 무엇과 다른가).
+//   validate:         counts of values no step of the method writes (a debug check, pace_validate_state).
 // One CTA per unit, one thread per column; groups are thread-local.
 #include "pace_common.cuh"
 
@@ -168,4 +169,110 @@ cudaError_t pace_launch_calib(const PaceDev &d, int bits, int group, int zero_po
                       : launch_calib_t<64, 1>(d, bits, group, zero_point, e_out, s);
   return d.D == 128 ? launch_calib_t<128, 0>(d, bits, group, zero_point, e_out, s)
                     : launch_calib_t<64, 0>(d, bits, group, zero_point, e_out, s);
+}
+
+// ---- pace_validate_state: every thread counts over grid-stride ranges, then one atomic add per warp and count
+namespace pace {
+
+struct ValidateArgs {
+  const char *base;
+  int n_guards;
+  size_t guard[PACE_MAX_GUARDS];
+  unsigned long long *counts;
+};
+
+__device__ __forceinline__ bool bf16_bits_nonfinite(uint32_t b) { return (b & 0x7F80u) == 0x7F80u; }
+
+__global__ void __launch_bounds__(256) validate_kernel(const PaceDev d, const ValidateArgs a) {
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x, nth = (size_t)gridDim.x * blockDim.x;
+  unsigned c[PACE_VALIDATE_N] = {};
+  const size_t U = (size_t)d.B * d.H, D = d.D, NG = d.NG, P = d.dP;
+  // [0] buffer counters
+  for (size_t u = tid; u < U; u += nth) {
+    const int m = d.m[u];
+    if (m < 0 || m >= d.dP) ++c[0];
+  }
+  if (d.state_mode == PACE_STATE_QUANT) {
+    // [1] scales: negative (non-zero), infinite or NaN
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(d.scale);
+    for (size_t i = tid; i < U * NG * D; i += nth) {
+      const uint32_t b = sc[i];
+      if (bf16_bits_nonfinite(b) || ((b & 0x8000u) && (b & 0x7FFFu))) ++c[1];
+    }
+    if (d.zero_point) {
+      // [2] zero points above the head's code range
+      for (size_t i = tid; i < U * NG * D; i += nth) {
+        const int h = (int)((i / (NG * D)) % (size_t)d.H);
+        if (d.zp[i] > (d.head_is_int8[h] ? 255 : 15)) ++c[2];
+      }
+    } else {
+      // [3] symmetric codes at the unused level (stored 0): int4 nibbles; int8 where both planes hold 0
+      const size_t W = D * D / 8;
+      for (size_t i = tid; i < (size_t)d.B * d.H4 * W; i += nth) {
+        const uint32_t w = d.codes4[i];
+        for (int k = 0; k < 8; ++k) c[3] += ((w >> (4 * k)) & 0xFu) == 0u;
+      }
+      for (size_t i = tid; i < (size_t)d.B * d.H8 * W; i += nth) {
+        const size_t u = i / W, r = i - u * W;
+        const uint32_t lo = d.codes8[(2 * u) * W + r], hi = d.codes8[(2 * u + 1) * W + r];
+        for (int k = 0; k < 8; ++k) c[3] += (((lo | hi) >> (4 * k)) & 0xFu) == 0u;
+      }
+    }
+  } else if (d.S) {
+    // [1] fp32 / bf16 state values that are infinite or NaN
+    const size_t n = U * D * D;
+    if (d.state_mode == PACE_STATE_FP32) {
+      const float *S = static_cast<const float *>(d.S);
+      for (size_t i = tid; i < n; i += nth) c[1] += !isfinite(S[i]);
+    } else {
+      const uint16_t *S = static_cast<const uint16_t *>(d.S);
+      for (size_t i = tid; i < n; i += nth) c[1] += bf16_bits_nonfinite(S[i]);
+    }
+  }
+  // [4] pending buffer entries (slots below m of units with a valid counter)
+  if (d.buf_s && d.state_mode != PACE_STATE_BF16) {
+    const bool keys = d.gamma == 1;
+    for (size_t i = tid; i < U * P; i += nth) {
+      const size_t u = i / P;
+      const int t = (int)(i - u * P), m = d.m[u];
+      if (m < 0 || m >= d.dP || t >= m) continue;
+      for (int e = 0; e < 4; ++e) c[4] += !isfinite(d.buf_s[i * 4 + e]);
+      if (d.buf_mode == PACE_BUF_FP32) {
+        const float *kr = static_cast<const float *>(d.buf_k) + i * D, *vr = static_cast<const float *>(d.buf_v) + i * D;
+        for (size_t j = 0; j < D; ++j) c[4] += (keys && !isfinite(kr[j])) + !isfinite(vr[j]);
+      } else if (d.buf_mode == PACE_BUF_MIXED) {
+        const uint8_t *kr = static_cast<const uint8_t *>(d.buf_k) + i * (D / 2);
+        const uint16_t *vr = static_cast<const uint16_t *>(d.buf_v) + i * D;
+        for (size_t j = 0; j < D / 2; ++j)
+          c[4] += keys ? ((kr[j] & 0xFu) == 0u) + ((kr[j] >> 4) == 0u) : 0u;
+        for (size_t j = 0; j < D; ++j) c[4] += bf16_bits_nonfinite(vr[j]);
+      } else {
+        const int8_t *kr = static_cast<const int8_t *>(d.buf_k) + i * D, *vr = static_cast<const int8_t *>(d.buf_v) + i * D;
+        for (size_t j = 0; j < D; ++j) c[4] += (keys && kr[j] == -128) + (vr[j] == -128);
+      }
+    }
+  }
+  // [5] guard bytes
+  for (int g = 0; g < a.n_guards; ++g)
+    for (size_t i = tid; i < PACE_GUARD_BYTES; i += nth) c[5] += (uint8_t)a.base[a.guard[g] + i] != 0xA5u;
+#pragma unroll
+  for (int k = 0; k < PACE_VALIDATE_N; ++k) {
+    unsigned v = c[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0 && v) atomicAdd(a.counts + k, (unsigned long long)v);
+  }
+}
+
+}  // namespace pace
+
+cudaError_t pace_launch_validate(const PaceDev &d, const char *base, const size_t *guard, int n_guards,
+                                 unsigned long long *counts, cudaStream_t s) {
+  pace::ValidateArgs a;
+  a.base = base;
+  a.n_guards = n_guards < PACE_MAX_GUARDS ? n_guards : PACE_MAX_GUARDS;
+  for (int g = 0; g < PACE_MAX_GUARDS; ++g) a.guard[g] = g < a.n_guards ? guard[g] : 0;
+  a.counts = counts;
+  pace::validate_kernel<<<pace::device_sm_count() * 4, 256, 0, s>>>(d, a);
+  return cudaGetLastError();
 }

@@ -58,6 +58,8 @@ enum { PACE_IO_BF16 = 0, PACE_IO_F32 = 1 };
 
 #define PACE_MAX_HEADS 256
 #define PACE_MAX_DP 32
+#define PACE_GUARD_BYTES 256   /* guard region after every array of a state region (pace_validate_state) */
+#define PACE_VALIDATE_N 6      /* counts pace_validate_state reports */
 
 /* Immutable configuration of one state ([P1] 무엇과 다른가, 어떻게 동작하나). */
 typedef struct {
@@ -97,7 +99,10 @@ typedef struct pace_state pace_state;   /* opaque host handle */
  *   buf_v   int8   [B][H][dP][d_v]      mixed: bf16 values; fp32 buffer: float
  *   buf_s   float  [B][H][dP][4]        a_t, beta_t, key scale, value scale
  *   m       int32  [B][H]               tokens in the buffer
- *   status  int32  [1]                  bit 0: a bounded device wait gave up (see pace_get_status)
+ *   status  int32  [64]                 word 0, bit 0: a bounded device wait gave up (see pace_get_status);
+ *                                      words 16..27: the counts of the last pace_validate_state
+ * Every array is followed by a PACE_GUARD_BYTES guard region, filled with 0xA5 when the state is allocated;
+ * pace_validate_state counts guard bytes that changed (a write past the end of an array).
  *   S       float/bf16 [B][H][d_k][d_v] state of PACE_STATE_FP32 / PACE_STATE_BF16 and PACE_STATE_BF16_BUF
  * head_slot[h] is the index of head h inside its pool (codes4 or codes8). */
 typedef struct {
@@ -197,6 +202,21 @@ pace_status pace_get_status(const pace_state *state, int clear, int *status_out,
  * unchanged, sets bit 0 of the status word (pace_get_status then returns PACE_ERR_TIMEOUT) and releases its
  * tensor memory. ns = 0 turns the probe off. Host-only; PACE_ERR_INVALID_ARG for a NULL state. */
 pace_status pace_test_wait_probe(pace_state *state, uint32_t ns);
+
+/* Debug check of a state: no value of the state changes and nothing can fault. Counts, over all units, into
+ * the HOST array counts_out[PACE_VALIDATE_N]:
+ *   [0] buffer counters m outside 0..dP-1;
+ *   [1] group scales that are negative, infinite or NaN (bf16 bits); in the fp32 and bf16 state modes, state
+ *       values that are infinite or NaN;
+ *   [2] zero points above the code range of their head (15 for an int4 head);
+ *   [3] symmetric codes at the unused level -2^(b-1) (stored as 0);
+ *   [4] values of pending buffer entries (slots below m) that no quantizer writes: an int8 code of -128, a
+ *       mixed-buffer int4 key stored as 0, a non-finite bf16 value, a non-finite a, beta or scale (key rows
+ *       shared by several value heads are not checked);
+ *   [5] guard bytes that differ from 0xA5.
+ * Launches one counting kernel on `stream` and SYNCHRONISES `stream` to read the counts. Returns
+ * PACE_ERR_STATE when any count is non-zero (counts_out is filled either way). */
+pace_status pace_validate_state(const pace_state *state, int64_t *counts_out, void *stream);
 
 /* Message for the last non-OK status returned to the calling thread ("" if none). */
 const char *pace_last_error(void);

@@ -5,7 +5,11 @@
   status word; the units and their outputs are unchanged, no MMA was issued, and the context stays usable (the
   same chunk then runs normally and matches the oracle).
 * A unit whose buffer counter is out of range (a corrupted region, built on the host and imported) is left
-  unchanged and its output is zero; every other unit decodes exactly as before."""
+  unchanged and its output is zero; every other unit decodes exactly as before.
+* pace_validate_state counts exactly the corrupt values planted in a host copy of the region (counter, scale,
+  zero point, unused code level, buffer entry, guard byte) and nothing in a clean state."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -93,3 +97,65 @@ def test_out_of_range_counter_leaves_unit_unchanged(P):
     for a0, a1 in zip(blob0.buffer(*bad), blob1.buffer(*bad)):
         assert np.array_equal(a0, a1)
     assert blob1.m()[bad] == wl.dP + 3
+
+
+def _export(P, state):
+    import torch
+    L = state.layout
+    host = torch.empty(L.total_bytes, dtype=torch.uint8).pin_memory()
+    P.pace_state_export(state.handle, host, host.numel())
+    torch.cuda.synchronize()
+    return host
+
+
+def _import(P, state, host):
+    import torch
+    P.pace_state_import(state.handle, host, host.numel())
+    torch.cuda.synchronize()
+
+
+def test_validate_state_counts_planted_corruption(P):
+    """pace_validate_state counts values that no step of the method writes. Each is planted in a host copy of
+    the region and imported; a clean state counts zero everywhere, the corrupted one exactly what was planted."""
+    wl = synth.workload("pace48", B=2, H=4)          # zero points, one int8 head, mixed buffer
+    mask = np.array([0, 1, 0, 0], np.uint8)
+    run = PairRun(wl, mask=mask)
+    run.prefill(256)
+    for _ in range(3):
+        run.decode()
+    clean = run.state.validate()
+    assert not any(clean.values()), clean
+    L, D, NG = run.state.layout, wl.d_k, wl.d_k // wl.g
+    host = _export(P, run.state)
+    raw = host.numpy()
+    raw[L.m:L.m + 4 * wl.B * wl.H].view(np.int32)[1] = wl.dP + 2           # [0] unit (0, 1): counter
+    raw[L.scale:L.scale + 2 * wl.B * wl.H * NG * D].view(np.uint16)[2 * NG * D] = 0x7FC0   # [1] unit 2: NaN scale
+    raw[L.zp] = 20                                                          # [2] int4 head 0: zero point 20
+    k3 = L.buf_k + (3 * wl.dP) * (D // 2)                                   # [4] unit 3, slot 0: key stored as 0
+    assert raw[k3] & 0x0F
+    raw[k3] &= 0xF0
+    raw[L.codes8 - 1] = 0                                                   # [5] the guard before codes8
+    _import(P, run.state, host)
+    got = run.state.validate()
+    want = dict(zip(P.VALIDATE_FIELDS, (1, 1, 1, 0, 1, 1)))
+    assert got == want, got
+    counts = (ctypes.c_int64 * P.PACE_VALIDATE_N)()
+    assert P.lib().pace_validate_state(run.state.handle, counts, None) == P.PACE_ERR_STATE
+    assert list(counts) == [1, 1, 1, 0, 1, 1]
+
+
+def test_validate_state_counts_unused_symmetric_level(P):
+    """Symmetric codes never take the level -2^(b-1) (stored 0): one planted int4 code at that level is counted."""
+    wl = synth.workload("pace4", B=2, H=2)
+    run = PairRun(wl)
+    run.prefill(256)
+    assert not any(run.state.validate().values())
+    host = _export(P, run.state)
+    raw = host.numpy()
+    c4 = run.state.layout.codes4
+    w = raw[c4:c4 + 4].view(np.uint32)
+    assert w[0] & 0xF
+    w[0] &= 0xFFFFFFF0
+    _import(P, run.state, host)
+    got = run.state.validate()
+    assert got == dict(zip(P.VALIDATE_FIELDS, (0, 0, 0, 1, 0, 0))), got
