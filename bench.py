@@ -47,6 +47,9 @@ def parse_args(argv=None):
     p.add_argument("--batch", type=int, default=64)
     p.add_argument("--extra", type=int, default=1, help="also time batch 128, the bf16 kernel and prefill")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle sample")
+    p.add_argument("--pace48-only", type=int, default=0, metavar="K",
+                   help="only time K steps of the PACE-4/8 leg (batch 128, 8 int8 heads by pace_assign_heads), print "
+                        "one JSON line and exit (a short command for profiling its two pool kernels)")
     p.add_argument("--prefill-only", type=int, default=0, metavar="B",
                    help="only time two 256-token prefill chunks on one PACE-4 state of B sequences x 32 heads "
                         "(a small case for profiling the chunk kernel), print one JSON line and exit")
@@ -649,7 +652,8 @@ def pace48_leg(P, torch, peak, K, W):
     return {"B": wl.B, "H": wl.H, "int8_heads": [int(h) for h in np.flatnonzero(mask)], "tokens_per_s": wl.B / (ms * 1e-3),
             "ms_per_step": ms, "bytes_per_unit_step": per, "achieved_gbs": alg / (ms * 1e-3) / 1e9,
             "frac": alg / (ms * 1e-3) / 1e9 / peak, "rotating_sets": R, "rounding_steps_in_window": rounding,
-            "steps": K, "note": "two launches per step (int4 pool, int8 pool)"}
+            "steps": K, "note": "two launches per step: the int4 pool, and the int8 pool on the state's own stream "
+                                "(forked and joined by events) so that both pools share the SMs"}
 
 
 def longctx_decode(P, torch, peak, K, W):
@@ -771,6 +775,10 @@ def main():
     torch.cuda.set_device(local)
     if args.prefill_only:
         prefill_only(P, torch, args.prefill_only)
+        return
+    if args.pace48_only:
+        peak, _ = read_peaks()
+        print(json.dumps({"pace48_only": pace48_leg(P, torch, peak, args.pace48_only, 3)}), flush=True)
         return
     dist = None
     if world > 1:

@@ -204,6 +204,9 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   constexpr bool BF = BITS == 16;
   constexpr int CPL = D / 32, NG = D / G, MT = D / 16, NPP = D / 64, PL = BF ? 1 : BITS / 4, KS = D / 16, KSG = G / 16;
   constexpr int RS = D + 16, YS = D + 8, MTW = MT / WU, CW = D / WU, CPW = CW / 32;
+  // the dot loop over M-tiles stays rolled except for the smallest tile body (int4, symmetric, two groups, int8
+  // buffer): the larger bodies, fully unrolled, overflow the instruction cache
+  constexpr bool DF_ROLL = !(BITS == 4 && NG <= 2 && !ZP && !MX);
   constexpr int OFF = BF ? 0 : 1 << (BITS - 1);
   constexpr int NKG = G / 8;
   static_assert(MTW >= 1 && CPW >= 1, "warps per unit");
@@ -579,8 +582,9 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     // rounding step, with twice the accumulators, takes one tile at a time)
     constexpr int TP = 1;
     static_assert(MTW % 2 == 0, "tiles are loaded in pairs");
-#pragma unroll
-    for (int mi = 0; mi < MTW; mi += TP) {
+    // one M-tile; PAR = the tile's parity, which selects its register buffer (cwA even, cwB odd)
+    auto tile = [&](const int mi, auto par) {
+      constexpr int PAR = decltype(par)::value;
       float ay[TP][NG][PL][4], ak[TP][NG][PL][4];
 #pragma unroll
       for (int tt = 0; tt < TP; ++tt)
@@ -602,7 +606,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
           for (int pp = 0; pp < NPP; ++pp) {
             const uint4 v = *reinterpret_cast<const uint4 *>(cs + (((mi + tt) * NPP + pp) * 32 + lane) * 4);
-            uint32_t(&w)[PL][NPP][4] = ((mi + tt) & 1) ? cwB : cwA;
+            uint32_t(&w)[PL][NPP][4] = (PAR ^ (tt & 1)) ? cwB : cwA;
             w[0][pp][0] = v.x;
             w[0][pp][1] = v.y;
             w[0][pp][2] = v.z;
@@ -619,7 +623,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
             for (int pl = 0; pl < PL; ++pl) {
               uint32_t a[4];
-              df_afrag<D, PL>(((mi + tt) & 1) ? cwB : cwA, pl, ks, a);
+              df_afrag<D, PL>((PAR ^ (tt & 1)) ? cwB : cwA, pl, ks, a);
               mma_f16(ay[tt][g][pl], a, yb[ks][0], yb[ks][1]);
               if (WK) mma_f16(ak[tt][g][pl], a, kb[ks][0], kb[ks][1]);
             }
@@ -628,7 +632,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       if (!SM) {
 #pragma unroll
         for (int tt = 0; tt < TP; ++tt)
-          if (mi + tt + 2 < MTW) df_load_tile<D, PL>(codes, mt0 + mi + tt + 2, lane, ((mi + tt) & 1) ? cwB : cwA);
+          if (mi + tt + 2 < MTW) df_load_tile<D, PL>(codes, mt0 + mi + tt + 2, lane, (PAR ^ (tt & 1)) ? cwB : cwA);
       }
 #pragma unroll
       for (int tt = 0; tt < TP; ++tt) {
@@ -679,6 +683,21 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
             pb[(t0 + 1) * D + j1] = pk[1][1];
           }
         }
+      }
+    };
+    // the tiles in pairs; a rolled loop where the unrolled one would overflow the instruction cache (more groups,
+    // zero points, the mixed buffer or int8 planes make the tile body several times larger)
+    if constexpr (DF_ROLL) {
+#pragma unroll 1
+      for (int mi = 0; mi < MTW; mi += 2) {
+        tile(mi, std::integral_constant<int, 0>{});
+        tile(mi + 1, std::integral_constant<int, 1>{});
+      }
+    } else {
+#pragma unroll
+      for (int mi = 0; mi < MTW; mi += 2) {
+        tile(mi, std::integral_constant<int, 0>{});
+        tile(mi + 1, std::integral_constant<int, 1>{});
       }
     }
   };
