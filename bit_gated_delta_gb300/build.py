@@ -15,6 +15,7 @@ LIB = os.path.join(PKG, "libpace.so")
 
 SOURCES = ["pace_api.cu", "decode.cu", "decode_mma_s8.cu", "decode_mma_sm.cu", "decode_mma_z8.cu", "decode_mma_zm.cu",
            "decode_fold_s8.cu", "decode_fold_sm.cu", "decode_fold_z8.cu", "decode_fold_zm.cu", "decode_fold_bf.cu",
+           "decode_fold_t32.cu",
            "decode_bf16.cu", "prefill.cu", "prefill_tc.cu", "state_ops.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

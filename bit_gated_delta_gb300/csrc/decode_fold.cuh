@@ -35,28 +35,36 @@ struct FoldSmem {
 };
 // Per-warp work area. int8 rows use a stride of D + 16 bytes and fp16 digit rows D + 8 halves, so that the
 // fragment loads of the eight rows of a tile fall in distinct banks.
-__host__ __device__ inline FoldSmem fold_smem(int D, int G, int mixed, int zp, int bf = 0) {
+__host__ __device__ inline FoldSmem fold_smem(int D, int G, int mixed, int zp, int bf = 0, int tk = DF_TOK) {
   FoldSmem L;
   size_t off = 0;
-  L.krow = carve(off, (size_t)11 * (D + 16));               // key codes of tokens 0..7, then the 3 digits of q
-  L.vrow = carve(off, (size_t)DF_TOK * D * (mixed ? 2 : 1)); // value codes (int8) or bf16 values
+  L.krow = carve(off, (size_t)(tk + 3) * (D + 16));         // key codes of tokens 0..tk-1, then the 3 digits of q
+  L.vrow = carve(off, (size_t)tk * D * (mixed ? 2 : 1));     // value codes (int8) or bf16 values
+  // 32-token tables: the Gram matrix and then L share one area, and the rounding step's key table is built after
+  // the replay over the values and that area (both dead by then), so that six units fit on an SM
+  if (tk > DF_TOK) L.gram = L.Lm = carve(off, (size_t)tk * tk * 4);
   L.ydig = carve(off, (size_t)3 * (D + 8) * 2);              // fp16 digit rows of y; packed int4 keys of the
                                                              // mixed buffer while staging
   L.ssc = carve(off, bf ? 0 : (size_t)(D / G) * D * 2);      // group scales (bf16), as resident
   L.szp = carve(off, zp ? (size_t)(D / G) * D : 0);          // zero points
   L.po = carve(off, (size_t)D * 4);                          // S_hat^T y per column
-  L.pb = carve(off, (size_t)DF_TOK * D * 4);                 // rounding step: P_t then u_t [t][j]
-  L.kbf = carve(off, (size_t)D * 4 * 4 * (bf ? 2 : 1));      // flush B operand: fp16 pairs of int8 keys [i][pair];
+  L.pb = carve(off, (size_t)tk * D * 4);                     // rounding step: P_t then u_t [t][j]
+  if (tk > DF_TOK) {
+    L.kbf = L.vrow;                                          // fp16 key pairs [i][tk/2], after the replay
+    L.csx = carve(off, 0);                                   // (pb alone holds the staged code words)
+  } else {
+    L.kbf = carve(off, (size_t)D * 4 * 4 * (bf ? 2 : 1));    // flush B operand: fp16 pairs of int8 keys [i][pair];
                                                              // bf16 state: the keys as fp32 [i][t] (kf)
-  // steps without a rounding: the unit's int4 code words are staged over pb, kbf and this spare area
-  L.csx = carve(off, !bf && (size_t)D * D / 2 > (L.kbf - L.pb) + (size_t)D * 16
-                         ? (size_t)D * D / 2 - (L.kbf - L.pb) - (size_t)D * 16 : 0);
+    // steps without a rounding: the unit's int4 code words are staged over pb, kbf and this spare area
+    L.csx = carve(off, !bf && (size_t)D * D / 2 > (L.kbf - L.pb) + (size_t)D * 16
+                           ? (size_t)D * D / 2 - (L.kbf - L.pb) - (size_t)D * 16 : 0);
+  }
   L.kf = L.kbf;
-  L.gram = carve(off, 64 * 4);                               // k_s.k_t (integers)
-  L.qk = carve(off, 3 * 8 * 4);                              // (q digit d).k_t (integers)
-  L.Lm = carve(off, 64 * 4);                                 // L[t][s]
-  L.tk = carve(off, DF_TOK * 16);                            // per token: G_t s_kt, beta_t, s_vt, 0
-  L.ck = carve(off, DF_TOK * 4);                             // flush coefficient (G_m/G_s) s_ks
+  if (tk <= DF_TOK) L.gram = carve(off, 64 * 4);             // k_s.k_t (integers)
+  L.qk = carve(off, 3 * (size_t)tk * 4);                     // (q digit d).k_t (integers)
+  if (tk <= DF_TOK) L.Lm = carve(off, 64 * 4);               // L[t][s]
+  L.tk = carve(off, (size_t)tk * 16);                        // per token: G_t s_kt, beta_t, s_vt, 0
+  L.ck = carve(off, (size_t)tk * 4);                         // flush coefficient (G_m/G_s) s_ks
   L.total = carve(off, 0, 16);
   return L;
 }
@@ -196,7 +204,7 @@ __device__ __forceinline__ void df_sum(const uint32_t (*b)[2], float (&t2)[2]) {
 
 // One unit: staging, tables, the folded readout and (at m = dP) the rounding. WU warps share the unit: each
 // stages it on its own and takes D/16/WU of its M-tiles.
-template <int D, int G, int BITS, int ZP, int MX, int WU>
+template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
 __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int unit, int has_token,
                         unsigned char *wsm, int part) {
   // BITS 4 or 8: the packed int4 / int8 state (PACE); BITS 16: the bf16 state of the buffered bf16 mode (row-major,
@@ -210,9 +218,12 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   constexpr int OFF = BF ? 0 : 1 << (BITS - 1);
   constexpr int NKG = G / 8;
   static_assert(MTW >= 1 && CPW >= 1, "warps per unit");
+  // TK: buffered tokens the tables hold (8, or 32 for the longer periods of the int4 symmetric state)
+  static_assert(TK == DF_TOK || (TK == 32 && BITS == 4 && !ZP && !MX), "32-token tables: int4 symmetric only");
+  constexpr int QR = TK;                           // first of the three q digit rows in krow
   const int lane = threadIdx.x & 31, g8 = lane >> 2, tq = lane & 3;
   const int dP = st.dP;
-  const FoldSmem L = fold_smem(D, G, MX, ZP, BF);
+  const FoldSmem L = fold_smem(D, G, MX, ZP, BF, TK);
   int8_t *krow = reinterpret_cast<int8_t *>(wsm + L.krow);
   unsigned char *vrow = wsm + L.vrow;
   __half *ydig = reinterpret_cast<__half *>(wsm + L.ydig);
@@ -344,9 +355,9 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       d2[c] = (q1 + 128) >> 8;
       d1[c] = q1 - (d2[c] << 8);
     }
-    dm_store_bytes<CPL>(krow + 8 * RS + col0, d2);
-    dm_store_bytes<CPL>(krow + 9 * RS + col0, d1);
-    dm_store_bytes<CPL>(krow + 10 * RS + col0, d0);
+    dm_store_bytes<CPL>(krow + QR * RS + col0, d2);
+    dm_store_bytes<CPL>(krow + (QR + 1) * RS + col0, d1);
+    dm_store_bytes<CPL>(krow + (QR + 2) * RS + col0, d0);
   }
   // the warp's first two code tiles, once the new token is in
   uint32_t cwA[PL][NPP][4], cwB[PL][NPP][4];
@@ -384,7 +395,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // ---- Gram products k_s.k_t and (q digit).k_t: fp16 MMA (the int8 codes and digits are exact in fp16, every sum
   // an exact integer below 2^24), A = [keys 0..7 | q digits] (M), B = keys (N). (An int8 MMA would take the codes as
   // they are, but on this chip it runs at an eighth of the fp16 rate.)
-  {
+  if constexpr (TK == DF_TOK) {
     float gacc[4][4] = {};   // four independent chains of the K steps
     const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;   // the lane's key pair inside its 4-byte load
 #pragma unroll
@@ -393,14 +404,48 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       uint32_t a[4];
       a[0] = i8pair_f16(lds32(krow + g8 * RS + off), sel, false);
       a[2] = i8pair_f16(lds32(krow + g8 * RS + off + 8), sel, false);
-      a[1] = g8 < 3 ? i8pair_f16(lds32(krow + (8 + g8) * RS + off), sel, false) : 0u;
-      a[3] = g8 < 3 ? i8pair_f16(lds32(krow + (8 + g8) * RS + off + 8), sel, false) : 0u;
+      a[1] = g8 < 3 ? i8pair_f16(lds32(krow + (QR + g8) * RS + off), sel, false) : 0u;
+      a[3] = g8 < 3 ? i8pair_f16(lds32(krow + (QR + g8) * RS + off + 8), sel, false) : 0u;
       mma_f16(gacc[ks & 3], a, a[0], a[2]);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) gacc[0][e] = (gacc[0][e] + gacc[1][e]) + (gacc[2][e] + gacc[3][e]);
     *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2(gacc[0][0], gacc[0][1]);
     if (g8 < 3) *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2(gacc[0][2], gacc[0][3]);
+  } else {
+    // 32 tokens: M tiles = tokens 0-15, tokens 16-31, the q digits; N tiles = 8 tokens each (only those in use)
+    const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;
+    const int nt = (mt + 7) >> 3;
+#pragma unroll 1
+    for (int nb = 0; nb < nt; ++nb) {
+      float gacc[3][4] = {};
+#pragma unroll 2
+      for (int ks = 0; ks < KS; ++ks) {
+        const int off = 16 * ks + 4 * (tq >> 1);
+        const int8_t *rb = krow + (8 * nb + g8) * RS + off;
+        const uint32_t b0 = i8pair_f16(lds32(rb), sel, false), b1 = i8pair_f16(lds32(rb + 8), sel, false);
+#pragma unroll
+        for (int ma = 0; ma < 3; ++ma) {
+          if (ma < 2 && 16 * ma >= mt) continue;
+          const int r0 = ma < 2 ? 16 * ma + g8 : QR + g8, r1 = 16 * ma + 8 + g8;
+          const bool v0 = ma < 2 || g8 < 3, v1 = ma < 2;
+          uint32_t a[4];
+          a[0] = v0 ? i8pair_f16(lds32(krow + r0 * RS + off), sel, false) : 0u;
+          a[2] = v0 ? i8pair_f16(lds32(krow + r0 * RS + off + 8), sel, false) : 0u;
+          a[1] = v1 ? i8pair_f16(lds32(krow + r1 * RS + off), sel, false) : 0u;
+          a[3] = v1 ? i8pair_f16(lds32(krow + r1 * RS + off + 8), sel, false) : 0u;
+          mma_f16(gacc[ma], a, b0, b1);
+        }
+      }
+      const int cn = 8 * nb + 2 * tq;              // the fragment's two token columns
+#pragma unroll
+      for (int ma = 0; ma < 2; ++ma) {
+        if (16 * ma >= mt) continue;
+        *reinterpret_cast<float2 *>(gram + (16 * ma + g8) * TK + cn) = make_float2(gacc[ma][0], gacc[ma][1]);
+        *reinterpret_cast<float2 *>(gram + (16 * ma + 8 + g8) * TK + cn) = make_float2(gacc[ma][2], gacc[ma][3]);
+      }
+      if (g8 < 3) *reinterpret_cast<float2 *>(qk + g8 * TK + cn) = make_float2(gacc[2][0], gacc[2][1]);
+    }
   }
   __syncwarp();
 
@@ -408,15 +453,21 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   const int s = lane;
   const float a_s = bs.x, beta_s = bs.y, sk_s = bs.z, sv_s = bs.w;
   float Gs = 1.0f, gmr = 1.0f;                     // G_s = a_1 .. a_s ; G_m / G_s
-  float Lc[DF_TOK];                                // L_ts = beta_t (G_t/G_s) s_ks s_kt (k_s.k_t), t > s
+  float Lc[TK];                                    // L_ts = beta_t (G_t/G_s) s_ks s_kt (k_s.k_t), t > s
   {
-    float grow[DF_TOK];
-    *reinterpret_cast<float4 *>(grow) = *reinterpret_cast<const float4 *>(gram + (s & 7) * 8);
-    *reinterpret_cast<float4 *>(grow + 4) = *reinterpret_cast<const float4 *>(gram + (s & 7) * 8 + 4);
+    float grow[TK];
+    if constexpr (TK == DF_TOK) {
+      *reinterpret_cast<float4 *>(grow) = *reinterpret_cast<const float4 *>(gram + (s & 7) * 8);
+      *reinterpret_cast<float4 *>(grow + 4) = *reinterpret_cast<const float4 *>(gram + (s & 7) * 8 + 4);
+    } else {
+#pragma unroll
+      for (int q4 = 0; q4 < TK / 4; ++q4)
+        *reinterpret_cast<float4 *>(grow + 4 * q4) = *reinterpret_cast<const float4 *>(gram + s * TK + 4 * q4);
+    }
     const float bsk = beta_s * sk_s;
     float p = 1.0f;                                // a_{s+1} .. a_t
 #pragma unroll
-    for (int t = 0; t < DF_TOK; ++t) {
+    for (int t = 0; t < TK; ++t) {
       const float at = __shfl_sync(0xffffffffu, a_s, t);
       const float bt = __shfl_sync(0xffffffffu, bsk, t);
       if (t <= s) Gs *= at;
@@ -426,15 +477,17 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
     }
   }
   const float Gm = __shfl_sync(0xffffffffu, Gs, mt - 1);
+  if constexpr (TK > DF_TOK) __syncwarp();         // every Gram row is read before L takes its place
   if (do_flush) {
     if (s < mt) {
       tk[s] = make_float4(Gs * sk_s, beta_s, MX ? 1.0f : sv_s, 0.0f);
       ckf[s] = gmr * sk_s;
 #pragma unroll
-      for (int t = 0; t < DF_TOK; ++t) Lm[t * 8 + s] = Lc[t];
+      for (int t = 0; t < TK; ++t) Lm[t * TK + s] = Lc[t];
     }
-    // the flush B operand: kbf[i][p] = fp16 pair (k_{2p,i}, k_{2p+1,i}), zero for tokens >= mt
-    if constexpr (!BF) {
+    // the flush B operand: kbf[i][p] = fp16 pair (k_{2p,i}, k_{2p+1,i}), zero for tokens >= mt (32-token
+    // tables: built after the replay, below)
+    if constexpr (!BF && TK == DF_TOK) {
       const int p = lane & 3, t0 = 2 * p;
       const bool z0 = t0 >= mt, z1 = t0 + 1 >= mt;
 #pragma unroll
@@ -456,10 +509,11 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   float cvs = 0.0f;                                // c_s times the value scale (value coefficient of token s)
   float wd0 = 0.0f, wd1 = 0.0f;                    // weights of the lane's two digit columns
   if (has_token) {
-    const float kq = (65536.0f * qk[s & 7] + 256.0f * qk[8 + (s & 7)] + qk[16 + (s & 7)]) * sq;
+    const int sq8 = TK == DF_TOK ? (s & 7) : s;
+    const float kq = (65536.0f * qk[sq8] + 256.0f * qk[TK + sq8] + qk[2 * TK + sq8]) * sq;
     float z = s < mt ? gmr * sk_s * kq : 0.0f;     // cq_s, then z_s of (I + L)^T z = cq
 #pragma unroll
-    for (int t = DF_TOK - 1; t >= 0; --t) {
+    for (int t = TK - 1; t >= 0; --t) {
       if (t < mt) {
         const float zt = __shfl_sync(0xffffffffu, z, t);
         if (s < t) z = fmaf(-Lc[t], zt, z);
@@ -472,7 +526,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
     for (int c = 0; c < CPL; ++c) y[c] = Gm * tin.qx[c];
 #pragma unroll
-    for (int t = 0; t < DF_TOK; ++t) {
+    for (int t = 0; t < TK; ++t) {
       if (t < mt) {
         const float at = __shfl_sync(0xffffffffu, al, t);
         uint32_t kw;
@@ -532,18 +586,22 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) yb[ks][0] = yb[ks][1] = 0u;
   }
-  // B fragments of the buffered keys (rounding step): token g8's keys as fp16, second halves / 16
+  // B fragments of the buffered keys (rounding step): token tok0 + g8's keys as fp16, second halves / 16 (32-token
+  // tables: one group of 8 tokens at a time, tok0 = 0, 8, 16, 24)
   uint32_t kb[KS][2];
-  if (!BF && do_flush) {
+  int tok0 = 0;
+  auto load_kb = [&]() {
+    const int tg = tok0 + g8;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      const uint32_t x0 = g8 < mt ? lds32(krow + g8 * RS + 16 * ks + 4 * (tq >> 1)) : 0u;
-      const uint32_t x1 = g8 < mt ? lds32(krow + g8 * RS + 16 * ks + 8 + 4 * (tq >> 1)) : 0u;
+      const uint32_t x0 = tg < mt ? lds32(krow + tg * RS + 16 * ks + 4 * (tq >> 1)) : 0u;
+      const uint32_t x1 = tg < mt ? lds32(krow + tg * RS + 16 * ks + 8 + 4 * (tq >> 1)) : 0u;
       const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;
       kb[ks][0] = i8pair_f16(x0, sel, false);
       kb[ks][1] = i8pair_f16(x1, sel, true);
     }
-  }
+  };
+  if (!BF && do_flush) load_kb();
 
   // ---- group offsets: the contribution of the zero level (symmetric: code offset; zero point: 0) and, for zero
   // points and int8 planes, the plain sums T2
@@ -562,6 +620,17 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       if (do_flush) df_sum<KSG>(kb + g * KSG, t2k[g]);
     }
   }
+  auto key_offsets = [&]() {                       // the key operand's offsets again (next token group)
+#pragma unroll
+    for (int g = 0; g < (BF ? 0 : NG); ++g) {
+#pragma unroll
+      for (int pl = 0; pl < PL; ++pl) {
+        const uint32_t w = (!ZP && (BITS == 4 || pl == 1)) ? 0x88888888u : 0u;
+        offk[g][pl][0] = offk[g][pl][1] = 0.0f;
+        df_offset<KSG>(w, kb + g * KSG, offk[g][pl]);
+      }
+    }
+  };
 
   // the L2 prefetch of the warp's other tiles, after the tables (requested earlier, it delays the staging loads)
   if (smem_codes) {
@@ -576,7 +645,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // loop, so that a step without a rounding carries none of the rounding step's work.
   auto dots = [&](auto with_keys) {
     constexpr bool WK = decltype(with_keys)::value;
-    const bool wy = WK ? has_token != 0 : true;   // (steps without a rounding always have a token)
+    const bool wy = WK ? has_token != 0 && tok0 == 0 : true;   // (steps without a rounding always have a token)
     // TP tiles at a time (two on steps without a rounding, from registers cwA, cwB): their accumulators of every
     // group are independent chains, issued interleaved so that the tensor pipe always has work from this warp (the
     // rounding step, with twice the accumulators, takes one tile at a time)
@@ -673,7 +742,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
           else if (tq == 1) po[j1] = o1;
         }
         if (WK) {
-          const int t0 = 2 * tq;
+          const int t0 = tok0 + 2 * tq;
           if (t0 < mt) {
             pb[t0 * D + j0] = pk[0][0];
             pb[t0 * D + j1] = pk[1][0];
@@ -771,8 +840,24 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       for (int c = 0; c < CPW; ++c) po[jb + c] = acc[c];
     }
   } else {
-    if (do_flush) dots(std::true_type{});
-    else dots(std::false_type{});
+    if (!do_flush) {
+      dots(std::false_type{});
+    } else if constexpr (TK == DF_TOK) {
+      dots(std::true_type{});
+    } else {
+      // 32-token tables: one pass over the warp's tiles per group of 8 buffered tokens (the first pass also
+      // contracts y); each later pass reloads its first two tiles (from L2) and the key fragments
+#pragma unroll 1
+      for (tok0 = 0; tok0 == 0 || tok0 < mt; tok0 += 8) {
+        if (tok0 > 0) {
+          load_kb();
+          key_offsets();
+          df_load_tile<D, PL>(codes, mt0, lane, cwA);
+          if (MTW > 1) df_load_tile<D, PL>(codes, mt0 + 1, lane, cwB);
+        }
+        dots(std::true_type{});
+      }
+    }
   }
   __syncwarp();
 
@@ -783,7 +868,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
     for (int c = 0; c < CPW; ++c) o[c] = po[jc + c];
 #pragma unroll
-    for (int t = 0; t < DF_TOK; ++t) {
+    for (int t = 0; t < TK; ++t) {
       if (t < mt) {
         const float cv = __shfl_sync(0xffffffffu, cvs, t);
         if (MX) {
@@ -803,6 +888,35 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   if (do_flush) {
     // ---- replay of the lane's columns: u_t = beta_t r_t - sum_{s<t} L_ts u_s, r_t = v_t - G_t s_kt P_t
     float u[DF_TOK][CPW];
+    if constexpr (TK > DF_TOK) {
+      // 32-token tables: u_t replaces P_t in pb as it is found (the lane's own columns, so no barrier)
+      const int8_t *v8 = reinterpret_cast<const int8_t *>(vrow);
+#pragma unroll 1
+      for (int t = 0; t < mt; ++t) {
+        const float4 tt = tk[t];
+        float acc[CPW];
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) acc[c] = tt.y * fmaf(-tt.x, pb[t * D + jc + c], tt.z * (float)v8[t * D + jc + c]);
+#pragma unroll 4
+        for (int s2 = 0; s2 < t; ++s2) {
+          const float l = Lm[t * TK + s2];
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) acc[c] = fmaf(-l, pb[s2 * D + jc + c], acc[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) pb[t * D + jc + c] = acc[c];
+      }
+      __syncwarp();
+      // the rounding's key table over the values and L (both read for the last time above): kbf[i][p] = fp16
+      // pair (k_{2p,i}, k_{2p+1,i}), p < TK/2, zero for tokens >= mt
+      for (int idx = lane; idx < D * (TK / 2); idx += 32) {
+        const int i = idx / (TK / 2), t0 = 2 * (idx - i * (TK / 2));
+        const float k0 = t0 < mt ? (float)krow[t0 * RS + i] : 0.0f;
+        const float k1 = t0 + 1 < mt ? (float)krow[(t0 + 1) * RS + i] : 0.0f;
+        const __half2 hk = __floats2half2_rn(k0, k1);
+        kbf[idx] = *reinterpret_cast<const uint32_t *>(&hk);
+      }
+    } else {
 #pragma unroll
     for (int t = 0; t < DF_TOK; ++t) {
       if (t < mt) {
@@ -816,7 +930,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
         }
 #pragma unroll
         for (int s2 = 0; s2 < t; ++s2) {
-          const float l = Lm[t * 8 + s2];
+          const float l = Lm[t * TK + s2];
 #pragma unroll
           for (int c = 0; c < CPW; ++c) acc[c] = fmaf(-l, u[s2][c], acc[c]);
         }
@@ -829,6 +943,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 #pragma unroll
         for (int c = 0; c < CPW; ++c) u[t][c] = 0.0f;
       }
+    }
     }
     __syncwarp();
 
@@ -865,7 +980,7 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       }
     } else {
     // ---- rounding of the warp's M-tiles: S_new^T[j][i] = sum_s rho_s u_sj k_si + G_m s_gj (u_ij - z_gj)
-    const int dpp = 8;
+    constexpr int KP = TK / 2;                     // token pairs in a row of the key table kbf
     uint32_t cwn[PL][NPP][4];                      // the next tile's words, requested one tile ahead
     df_load_tile<D, PL>(codes, mt0, lane, cwn);
 #pragma unroll 1
@@ -883,28 +998,66 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
       // that puts the column's largest |rho_s u_s,j| in [2^8, 2^9), as two fp16 parts (about 22 significant bits;
       // K = 16 = 8 tokens x 2 parts, one MMA per key tile). The old state is scaled by the same 2^e_j, so the
       // accumulator holds 2^e_j x; scales and codes are invariant under it (the scale found is divided back).
-      uint32_t ap[2][2];
+      uint32_t a16[TK / 8][4];                     // one A fragment per group of 8 tokens
       float pw2[2], pw2i[2];
+      if constexpr (TK == DF_TOK) {
+        uint32_t ap[2][2];
 #pragma unroll
-      for (int hi = 0; hi < 2; ++hi) {
-        const int j = 16 * mtile + g8 + 8 * hi, s0 = 2 * tq;
-        float x0 = s0 < mt ? ckf[s0] * pb[s0 * D + j] : 0.0f;
-        float x1 = s0 + 1 < mt ? ckf[s0 + 1] * pb[(s0 + 1) * D + j] : 0.0f;
-        float mx = fmaxf(fabsf(x0), fabsf(x1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const int e = min(max(135 - (int)((__float_as_uint(mx) >> 23) & 0xFFu), -60), 60);
-        pw2[hi] = __uint_as_float((uint32_t)(e + 127) << 23);
-        pw2i[hi] = __uint_as_float((uint32_t)(127 - e) << 23);
-        x0 *= pw2[hi];
-        x1 *= pw2[hi];
-        const __half2 p0 = __floats2half2_rn(x0, x1);
-        const float2 f0 = __half22float2(p0);
-        const __half2 p1 = __floats2half2_rn(x0 - f0.x, x1 - f0.y);
-        ap[0][hi] = *reinterpret_cast<const uint32_t *>(&p0);
-        ap[1][hi] = *reinterpret_cast<const uint32_t *>(&p1);
+        for (int hi = 0; hi < 2; ++hi) {
+          const int j = 16 * mtile + g8 + 8 * hi, s0 = 2 * tq;
+          float x0 = s0 < mt ? ckf[s0] * pb[s0 * D + j] : 0.0f;
+          float x1 = s0 + 1 < mt ? ckf[s0 + 1] * pb[(s0 + 1) * D + j] : 0.0f;
+          float mx = fmaxf(fabsf(x0), fabsf(x1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const int e = min(max(135 - (int)((__float_as_uint(mx) >> 23) & 0xFFu), -60), 60);
+          pw2[hi] = __uint_as_float((uint32_t)(e + 127) << 23);
+          pw2i[hi] = __uint_as_float((uint32_t)(127 - e) << 23);
+          x0 *= pw2[hi];
+          x1 *= pw2[hi];
+          const __half2 p0 = __floats2half2_rn(x0, x1);
+          const float2 f0 = __half22float2(p0);
+          const __half2 p1 = __floats2half2_rn(x0 - f0.x, x1 - f0.y);
+          ap[0][hi] = *reinterpret_cast<const uint32_t *>(&p0);
+          ap[1][hi] = *reinterpret_cast<const uint32_t *>(&p1);
+        }
+        a16[0][0] = ap[0][0];
+        a16[0][1] = ap[0][1];
+        a16[0][2] = ap[1][0];
+        a16[0][3] = ap[1][1];
+      } else {
+        // 32 tokens: the column's exponent from all of its tokens, then one fragment per group of 8
+        float xs[TK / 8][2][2], mxh[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int q = 0; q < TK / 8; ++q)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int j = 16 * mtile + g8 + 8 * hi, s0 = 8 * q + 2 * tq;
+            xs[q][hi][0] = s0 < mt ? ckf[s0] * pb[s0 * D + j] : 0.0f;
+            xs[q][hi][1] = s0 + 1 < mt ? ckf[s0 + 1] * pb[(s0 + 1) * D + j] : 0.0f;
+            mxh[hi] = fmax3(mxh[hi], fabsf(xs[q][hi][0]), fabsf(xs[q][hi][1]));
+          }
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          float mx = mxh[hi];
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          const int e = min(max(135 - (int)((__float_as_uint(mx) >> 23) & 0xFFu), -60), 60);
+          pw2[hi] = __uint_as_float((uint32_t)(e + 127) << 23);
+          pw2i[hi] = __uint_as_float((uint32_t)(127 - e) << 23);
+        }
+#pragma unroll
+        for (int q = 0; q < TK / 8; ++q)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const float x0 = xs[q][hi][0] * pw2[hi], x1 = xs[q][hi][1] * pw2[hi];
+            const __half2 p0 = __floats2half2_rn(x0, x1);
+            const float2 f0 = __half22float2(p0);
+            const __half2 p1 = __floats2half2_rn(x0 - f0.x, x1 - f0.y);
+            a16[q][hi] = *reinterpret_cast<const uint32_t *>(&p0);
+            a16[q][2 + hi] = *reinterpret_cast<const uint32_t *>(&p1);
+          }
       }
-      const uint32_t a16[4] = {ap[0][0], ap[0][1], ap[1][0], ap[1][1]};
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
         float fs[2], fz[2];
@@ -917,8 +1070,11 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
         float c[NKG][4];
 #pragma unroll
         for (int nn = 0; nn < NKG; ++nn) {
-          const uint32_t bk = kbf[(8 * (gi * NKG + nn) + g8) * (dpp >> 1) + tq];
-          mma_f16_z(c[nn], a16, bk, bk);
+          const uint32_t *kr = kbf + (8 * (gi * NKG + nn) + g8) * KP + tq;
+          mma_f16_z(c[nn], a16[0], kr[0], kr[0]);
+#pragma unroll
+          for (int q = 1; q < TK / 8; ++q)
+            if (8 * q < mt) mma_f16(c[nn], a16[q], kr[4 * q], kr[4 * q]);
         }
         // the old state: 2^e_j x = 2^e_j G_m s_gj (u_ij - z_gj) + replay term, fp32 pairs (u - z exact)
 #pragma unroll
@@ -1026,8 +1182,8 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 }
 
 // One unit per block of WU warps; one launch per code pool (int4 heads, int8 heads).
-template <int D, int G, int BITS, int ZP, int MX, int WU>
-__global__ void __launch_bounds__(WU * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : BITS == 16 ? 16 : 12) / WU)
+template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
+__global__ void __launch_bounds__(WU * 32, (TK > DF_TOK ? 8 : BITS == 4 ? PACE_DM_MIN_WARPS : BITS == 16 ? 16 : 12) / WU)
     decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_enter();
@@ -1037,19 +1193,19 @@ __global__ void __launch_bounds__(WU * 32, (BITS == 4 ? PACE_DM_MIN_WARPS : BITS
   if (w >= st.B * HP) return;
   const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 8 ? st.H4 : 0) + slot];
-  const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16);
-  df_unit<D, G, BITS, ZP, MX, WU>(st, io, b, h, b * st.H + h, has_token, smem + (size_t)warp * L.total, warp);
+  const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16, TK);
+  df_unit<D, G, BITS, ZP, MX, WU, TK>(st, io, b, h, b * st.H + h, has_token, smem + (size_t)warp * L.total, warp);
 }
 
-template <int D, int G, int BITS, int ZP, int MX, int WU>
+template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
 static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, long units) {
-  const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16);
+  const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16, TK);
   const size_t smem = (size_t)WU * L.total;
-  cudaError_t e = smem_opt_in<decode_fold_kernel<D, G, BITS, ZP, MX, WU>>(smem);
+  cudaError_t e = smem_opt_in<decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(WU * 32), smem, s, attr);
-  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU>, d, io, has_token);
+  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>, d, io, has_token);
 }
 
 // Warps per unit by the size of the pool: while the units fill fewer than a half (a quarter) of the SMs' warp

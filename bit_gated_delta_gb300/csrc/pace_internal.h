@@ -59,6 +59,10 @@ struct PaceIO {
 cudaError_t pace_launch_decode(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_quant(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStream_t s);
+// The folded-readout kernel with 32-token tables (decode_fold_t32.cu): int4 symmetric, g = 64, int8 buffer, no int8
+// heads, 8 < dP <= 32.
+bool pace_fold32_supported(const PaceDev &d);
+cudaError_t pace_launch_decode_fold32(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 // Buffered bf16 state with dP <= 8 on the folded-readout kernel (decode_fold.cuh).
 cudaError_t pace_launch_decode_bf16buf_fold(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s);
 cudaError_t pace_launch_prefill(const PaceDev &d, const PaceIO &io, cudaStream_t s);
