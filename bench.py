@@ -801,7 +801,7 @@ def main():
     traffic = recorded_traffic("decode_fold_kernel", f"pace4_b{wl.B}")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS,
-                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_fold_kernel<128,64,4,0,0,1>",
+                "traffic": traffic, "peak_kind": peak_kind, "kernel": "pace::decode_fold_kernel<128,64,4,0,0,1,8>",
                 "algorithmic_bytes_per_launch": alg,
                 "note": "one decode_fold_kernel launch per step; duration = event time of K graph-replayed steps / K; "
                         "algorithmic bytes averaged over a rounding period"}
