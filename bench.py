@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -321,7 +322,11 @@ def time_e2e(torch, P, setup, K):
     """Same metric through the public API with host buffers: per step, one pinned host -> device copy of the
     step's packed inputs (q, k, v, a, beta back to back, each at a 16-byte aligned offset, as a model's fused
     projection would hand them over), the decode call on views of that buffer, and the device -> host copy of o,
-    all inside the timed region."""
+    all inside the timed region. The steps are pipelined as a serving loop would run them: the input copy on a
+    copy stream into one of two device buffers, the decode on the main stream, the output copy on a third stream
+    from one of two output buffers, ordered by events (a buffer is refilled only after the step that used it is
+    done), and the loop of G steps is captured once as a CUDA graph and replayed. The same steps issued one after
+    the other on one stream, without a graph, are timed too (serial_ms_per_step)."""
     wl = setup.wl
     names = ("q", "k", "v", "a", "beta")
     x0 = setup.inputs[0]
@@ -338,35 +343,90 @@ def time_e2e(torch, P, setup, K):
             n = v.numel() * v.element_size()
             hb[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8).cpu())
         host.append(hb)
-    dbuf = torch.empty(total, dtype=torch.uint8, device="cuda")
-    dev = {}
-    for k in names:
-        v = x0[k]
-        n = v.numel() * v.element_size()
-        dev[k] = dbuf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
-    o_host = torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16).pin_memory()
+    dbuf = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    dev = []
+    for j in range(2):
+        d = {}
+        for k in names:
+            v = x0[k]
+            n = v.numel() * v.element_size()
+            d[k] = dbuf[j][offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
+        dev.append(d)
+    obuf = [torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    o_host = [torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sum(x0[k].numel() * x0[k].element_size() for k in names)
-    d2h = o_host.numel() * o_host.element_size()
+    d2h = o_host[0].numel() * o_host[0].element_size()
     n = min(K, 2000)
+
+    # serial: each step's three operations back to back on one stream, issued from Python
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record()
     for i in range(n):
-        dbuf.copy_(host[i % DecodeSetup.NI], non_blocking=True)
-        setup.states[i % setup.R].decode_step(dev["q"], dev["k"], dev["v"], dev["a"], dev["beta"], setup.o)
-        o_host.copy_(setup.o, non_blocking=True)
+        dbuf[0].copy_(host[i % DecodeSetup.NI], non_blocking=True)
+        d = dev[0]
+        setup.states[i % setup.R].decode_step(d["q"], d["k"], d["v"], d["a"], d["beta"], obuf[0])
+        o_host[0].copy_(obuf[0], non_blocking=True)
     ev1.record()
     torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / n
-    # the host-to-device copy alone, the same packed pinned buffers back to back: the rate that bounds the leg
+    ms_serial = ev0.elapsed_time(ev1) / n
+
+    # pipelined and captured: G steps per graph (a multiple of the rotating sets and of the distinct inputs)
+    G = setup.R * DecodeSetup.NI // math.gcd(setup.R, DecodeSetup.NI)
+    while G < 16:
+        G *= 2
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_dec = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        main = torch.cuda.current_stream()
+        for e in ev_dec + ev_out:
+            e.record(main)
+        cin.wait_stream(main)
+        cout.wait_stream(main)
+        for i in range(G):
+            b = i & 1
+            cin.wait_event(ev_dec[b])              # the decode that read this input buffer is done
+            with torch.cuda.stream(cin):
+                dbuf[b].copy_(host[i % DecodeSetup.NI], non_blocking=True)
+            ev_in[b].record(cin)
+            main.wait_event(ev_in[b])
+            main.wait_event(ev_out[b])             # the copy-out of this output buffer is done
+            d = dev[b]
+            setup.states[i % setup.R].decode_step(d["q"], d["k"], d["v"], d["a"], d["beta"], obuf[b], main)
+            ev_dec[b].record(main)
+            cout.wait_event(ev_dec[b])
+            with torch.cuda.stream(cout):
+                o_host[b].copy_(obuf[b], non_blocking=True)
+            ev_out[b].record(cout)
+        main.wait_stream(cin)
+        main.wait_stream(cout)
+    reps = max(1, n // G)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(reps):
+        graph.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / (reps * G)
+    # the host-to-device copy alone, the same packed pinned buffers back to back
     ev0.record()
     for i in range(n):
-        dbuf.copy_(host[i % DecodeSetup.NI], non_blocking=True)
+        dbuf[0].copy_(host[i % DecodeSetup.NI], non_blocking=True)
     ev1.record()
     torch.cuda.synchronize()
     ms_copy = ev0.elapsed_time(ev1) / n
     return {"value": wl.B / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "steps": n, "note": "one packed host-to-device copy per step",
+            "ms_per_step": ms, "steps": reps * G,
+            "note": "per step: one packed pinned host-to-device copy (copy stream, two device buffers), the "
+                    "pace_decode_step call, the device-to-host copy of o (third stream, two pinned buffers); "
+                    f"{G} steps captured as one CUDA graph and replayed",
+            "serial_ms_per_step": ms_serial, "serial_note": "the same three operations per step on one stream, "
+                                                            "issued from Python without a graph",
             "h2d_copy_alone_ms": ms_copy, "h2d_copy_alone_gbs": total / (ms_copy * 1e-3) / 1e9}
 
 
