@@ -318,7 +318,7 @@ class _Null:
         return False
 
 
-def time_e2e(torch, P, setup, K):
+def time_e2e(torch, P, setup, K, nbuf=2):
     """Same metric through the public API with host buffers: per step, one pinned host -> device copy of the
     step's packed inputs (q, k, v, a, beta back to back, each at a 16-byte aligned offset, as a model's fused
     projection would hand them over), the decode call on views of that buffer, and the device -> host copy of o,
@@ -343,17 +343,17 @@ def time_e2e(torch, P, setup, K):
             n = v.numel() * v.element_size()
             hb[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8).cpu())
         host.append(hb)
-    dbuf = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    dbuf = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(nbuf)]
     dev = []
-    for j in range(2):
+    for j in range(nbuf):
         d = {}
         for k in names:
             v = x0[k]
             n = v.numel() * v.element_size()
             d[k] = dbuf[j][offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
         dev.append(d)
-    obuf = [torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    o_host = [torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    obuf = [torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
+    o_host = [torch.empty(wl.B, wl.H, wl.d_v, dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
     h2d = sum(x0[k].numel() * x0[k].element_size() for k in names)
     d2h = o_host[0].numel() * o_host[0].element_size()
     n = min(K, 2000)
@@ -376,9 +376,9 @@ def time_e2e(torch, P, setup, K):
     while G < 16:
         G *= 2
     cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_dec = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_dec = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         main = torch.cuda.current_stream()
@@ -387,7 +387,7 @@ def time_e2e(torch, P, setup, K):
         cin.wait_stream(main)
         cout.wait_stream(main)
         for i in range(G):
-            b = i & 1
+            b = i % nbuf
             cin.wait_event(ev_dec[b])              # the decode that read this input buffer is done
             with torch.cuda.stream(cin):
                 dbuf[b].copy_(host[i % DecodeSetup.NI], non_blocking=True)

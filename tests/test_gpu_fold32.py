@@ -60,3 +60,19 @@ def test_explicit_flush_and_prefill_after_pending_tokens(P):
     ok, msg = run.out_ok(g, r)
     assert ok, f"prefill after 5 pending tokens: {msg}"
     run.check_round_and_sync("prefill after pending decode")
+
+
+def test_shared_key_heads(P):
+    """Two value heads per key head (one buffered key row per key head) with 32-token tables."""
+    wl = synth.workload("pace4", B=4, H=8)
+    run = PairRun(wl, dP=24, key_heads=4)
+    g, r = run.prefill(256)
+    ok, msg = run.out_ok(g, r)
+    assert ok, f"prefill: {msg}"
+    run.check_round_and_sync("prefill")
+    for step in range(2 * 24 + 2):
+        g, r = run.decode()
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"step {step}: {msg}"
+        if (step + 1) % 24 == 0:
+            run.check_round_and_sync(f"step {step}")
