@@ -719,7 +719,8 @@ def pace48_leg(P, torch, peak, K, W):
 def longctx_decode(P, torch, peak, K, W):
     """Decode of the long-context shape (48 heads, d=128, batch 16, PACE-4 g=64) at rounding periods dP = 1, 8, 32,
     after a 512-token prefill (the decode cost does not depend on the context length: the state has a fixed size);
-    rotating state sets as in the default line. dP <= 8 runs the folded-readout kernel, dP = 32 the general one."""
+    rotating state sets as in the default line. Every period runs the folded-readout kernel (dP = 32 with its
+    32-token tables)."""
     import synth
     out = {}
     for dP in (1, 8, 32):

@@ -28,7 +28,7 @@
 
 namespace pace {
 
-constexpr int DF_TOK = 8;   // buffered tokens per unit this kernel handles (dP <= 8)
+constexpr int DF_TOK = 8;   // buffered tokens the tables hold by default (dP <= 8; 32-token tables: decode_fold_t32.cu)
 
 struct FoldSmem {
   size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, csx, kf, gram, qk, Lm, tk, ck, total;
