@@ -55,6 +55,10 @@ __host__ __device__ inline size_t carve(size_t &off, size_t bytes, size_t align 
 // as every block of this one has started (its blocks take SMs as ours leave), and a kernel touches no global
 // memory before every kernel it depends on has completed with its writes visible. Without the launch
 // attribute both instructions are no-ops.
+// Programmatic dependent launch in two halves: the trigger lets the next launch on the stream place its blocks, the
+// wait holds until the previous launch has finished and its writes are visible.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
