@@ -449,6 +449,11 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   }
   __syncwarp();
 
+  // the next launch on the stream may place its blocks from here (programmatic dependent launch): at entry they
+  // would crowd the SMs of a small launch while its units stage (measured on the 16-head layer shape, per launch
+  // at 48 / 128 / 256 units: trigger at entry 6.57 / 6.69 / 6.78 us, at the end of the unit 5.17 / 5.37 / 5.65, here
+  // 4.88 / 5.06 / 5.38; at 512-4096 units here and at entry are within 1%)
+  pdl_trigger();
   // ---- per-token tables (lane s = token s): decay products, L's column s, the flush coefficient
   const int s = lane;
   const float a_s = bs.x, beta_s = bs.y, sk_s = bs.z, sv_s = bs.w;
@@ -1184,14 +1189,9 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 // One unit per block of WU warps; one launch per code pool (int4 heads, int8 heads).
 template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
 __global__ void __launch_bounds__(WU * 32, (TK > DF_TOK ? 8 : BITS == 4 ? PACE_DM_MIN_WARPS : BITS == 16 ? 16 : 12) / WU)
-    decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token, const int late_trigger) {
+    decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token) {
   extern __shared__ __align__(128) unsigned char smem[];
-  // A launch with more units than two per SM lets the next launch place its blocks from the start, so they are
-  // resident when this one drains; a smaller launch (most SMs idle) triggers only as its blocks finish, so that
-  // waiting blocks do not crowd the SMs that running ones use (measured on the 16-head layer shape: at 48 and 256
-  // units the early trigger cost 27% and 19% per launch, at 512-4096 units the late one 1-2%).
-  if (!late_trigger) pdl_trigger();
-  pdl_wait();
+  pdl_wait();                                      // (the trigger follows the unit's Gram products, in df_unit)
   const int warp = threadIdx.x >> 5;
   const int HP = BITS == 8 ? st.H8 : st.H4;   // (the bf16 state: every head, in the first pool)
   const int w = blockIdx.x;
@@ -1200,7 +1200,6 @@ __global__ void __launch_bounds__(WU * 32, (TK > DF_TOK ? 8 : BITS == 4 ? PACE_D
   const int h = st.pool_head[(BITS == 8 ? st.H4 : 0) + slot];
   const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16, TK);
   df_unit<D, G, BITS, ZP, MX, WU, TK>(st, io, b, h, b * st.H + h, has_token, smem + (size_t)warp * L.total, warp);
-  if (late_trigger) pdl_trigger();
 }
 
 template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
@@ -1211,8 +1210,7 @@ static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_tok
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(WU * 32), smem, s, attr);
-  const int late = units <= 2L * device_sm_count();
-  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>, d, io, has_token, late);
+  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>, d, io, has_token);
 }
 
 // Warps per unit by the size of the pool: while the units fill fewer than a half (a quarter) of the SMs' warp
