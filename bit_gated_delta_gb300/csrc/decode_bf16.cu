@@ -15,9 +15,9 @@ __global__ void __launch_bounds__(2 * D) decode_bf16_kernel(const PaceDev st, co
   constexpr int RB = D / 4;           // rows per row block
   __shared__ float ks[D], qs[D], vs[D], us[D];
   __shared__ float part[4][D];
-  // the next launch's blocks: placed as this launch finishes when it has 33 units to two per SM, else from the start
+  // the next launch's blocks: placed as this launch finishes when it has 33 units to one per SM, else from the start
   // (measured on the 16-head layer shape: at 48 and 128 units the early trigger cost 16% and 12% per launch; at 16
-  // units the late one 6%, at 256 units the two are equal, above it the early one is ahead)
+  // units the late one 6%; at 256 units the two measured equal, above it the early one is ahead)
   if (!late_trigger) pdl_trigger();
   pdl_wait();
   const long unit = blockIdx.x;
@@ -77,7 +77,7 @@ cudaError_t pace_launch_decode_bf16(const PaceDev &d, const PaceIO &io, cudaStre
   if (units == 0) return cudaSuccess;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pdl_config(dim3(units), dim3(2 * d.D), 0, s, attr);
-  const int late = units > 32 && units <= 2u * (unsigned)device_sm_count();
+  const int late = units > 32 && units <= (unsigned)device_sm_count();
   return d.D == 128 ? cudaLaunchKernelEx(&cfg, decode_bf16_kernel<128>, d, io, late)
                     : cudaLaunchKernelEx(&cfg, decode_bf16_kernel<64>, d, io, late);
 }
