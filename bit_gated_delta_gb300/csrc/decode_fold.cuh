@@ -7,7 +7,7 @@
 // The output of the step does not need u. With cq_s = (G_m/G_s) k_s.q and c = diag(beta) (I + L)^-T cq,
 //   o = S_m^T q = G_m S_hat^T q + sum_s cq_s u_s = S_hat^T y + V^T c,   y = G_m q - sum_t c_t G_t k_t,
 // so a step without a rounding reads the packed state once against a single vector y. The per-unit work is an
-// 8 x 8 Gram matrix of the buffered int8 keys (fp16 tensor-core MMAs, 16 keys each, exact in fp32), a back
+// m x m Gram matrix of the buffered int8 keys (fp16 tensor-core MMAs, 16 keys each, exact in fp32), a back
 // substitution across lanes, and y; the state is then contracted with y's three int8 digits (a 24-bit fixed-point
 // image) on the tensor cores, straight from the packed nibbles:
 //   M = state columns (A: the lane's own packed words as fp16 1024 + u, or 1024 + 16u for the second 8 keys of a
@@ -20,6 +20,8 @@
 // The same kernel with BITS = 16 serves the buffered bf16 state (int8 decode buffer, bf16 state rounded to bf16
 // once every dP tokens): the prologue (token quantization, Gram, solve, y in fp32) is shared; the state is then read
 // on the CUDA cores, a row of D bf16 values per warp load, against y (and, at a rounding, against the buffered keys).
+// With TK = 32 the tables hold up to 32 buffered tokens (int4 symmetric state, periods of 9 to 32): the Gram
+// matrix over token tiles, a 32-lane solve, and a rounding that passes over the state once per group of 8 tokens.
 #pragma once
 
 #include <type_traits>
