@@ -65,6 +65,27 @@ def test_pace4_batch64_bench_configuration(P):
     assert (read_blob(run.state).m() == 0).all()
 
 
+def test_pace4_batch128_target_configuration(P):
+    """The target shape (batch 128, 32 heads, d=128, dP=8): 4,096 units, one warp each, in two waves; bf16 I/O,
+    the tensor-core prefill over all units, then 64 decode steps (eight roundings), 8 sampled units held to the
+    same bars as the batch-64 configuration."""
+    wl = synth.workload("pace4", B=128)
+    sample = [(0, 0), (17, 31), (63, 5), (64, 0), (90, 12), (101, 27), (126, 20), (127, 31)]
+    run = PairRun(wl, sample=sample)
+    for c in range(wl.prefill // 256):
+        g, r = run.prefill(256)
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"chunk {c}: {msg}"
+        run.check_round_and_sync(f"chunk {c}")
+    for step in range(8 * wl.dP):
+        g, r = run.decode()
+        ok, msg = run.out_ok(g, r)
+        assert ok, f"step {step}: {msg}"
+        if (step + 1) % wl.dP == 0:
+            run.check_round_and_sync(f"step {step}")
+    assert (read_blob(run.state).m() == 0).all()
+
+
 def test_pace4_two_warps_per_unit(P):
     """Batch 24 x 32 heads = 768 units fill fewer than half the warp slots, so two warps share each unit (each
     stages it and takes two of its four column blocks); outputs within the bar, codes of every rounding agree."""
