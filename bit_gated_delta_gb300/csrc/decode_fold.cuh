@@ -1191,15 +1191,35 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 // One unit per block of WU warps; one launch per code pool (int4 heads, int8 heads).
 template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
 __global__ void __launch_bounds__(WU * 32, (TK > DF_TOK ? 8 : BITS == 4 ? PACE_DM_MIN_WARPS : BITS == 16 ? 16 : 12) / WU)
-    decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token) {
+    decode_fold_kernel(const PaceDev st, const PaceIO io, const int has_token, const int one_wave) {
   extern __shared__ __align__(128) unsigned char smem[];
-  pdl_wait();                                      // (the trigger follows the unit's Gram products, in df_unit)
   const int warp = threadIdx.x >> 5;
   const int HP = BITS == 8 ? st.H8 : st.H4;   // (the bf16 state: every head, in the first pool)
   const int w = blockIdx.x;
-  if (w >= st.B * HP) return;
+  if (w >= st.B * HP) {
+    pdl_wait();
+    return;
+  }
   const int b = w / HP, slot = w - b * HP;
   const int h = st.pool_head[(BITS == 8 ? st.H4 : 0) + slot];
+  // Before the wait on the previous launch: L2 prefetches of the unit's first loads (its count and the new token),
+  // for a launch whose blocks are all resident at once (they may be placed while the previous launch drains). L2 is
+  // where device memory is coherent, so a line the previous launch writes afterwards is still read current.
+  // (Measured: -1.8% per step at 2,048 units, -2% at 48 and 1,024; with two waves, +1.6%, so not there.)
+  if (one_wave && warp == 0 && has_token) {
+    const int lane = threadIdx.x & 31, unit = b * st.H + h;
+    const size_t ku = (size_t)key_unit(st, unit);
+    const int es = st.io == PACE_IO_F32 ? 4 : 2;
+    const size_t c16 = (size_t)unit * 4 & ~(size_t)15;         // the 16 bytes holding the unit's word
+    const bool in16 = c16 + 16 <= (size_t)st.B * st.H * 4;       // (only where they lie inside the array)
+    if (lane == 0 && in16) prefetch_l2(reinterpret_cast<const char *>(st.m) + c16, 16);
+    else if (lane == 1) prefetch_l2(static_cast<const char *>(io.q) + ku * D * es, D * es);
+    else if (lane == 2) prefetch_l2(static_cast<const char *>(io.k) + ku * D * es, D * es);
+    else if (lane == 3) prefetch_l2(static_cast<const char *>(io.v) + (size_t)unit * D * es, D * es);
+    else if (lane == 4 && in16) prefetch_l2(reinterpret_cast<const char *>(io.a) + c16, 16);
+    else if (lane == 5 && in16) prefetch_l2(reinterpret_cast<const char *>(io.beta) + c16, 16);
+  }
+  pdl_wait();                                      // (the trigger follows the unit's Gram products, in df_unit)
   const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16, TK);
   df_unit<D, G, BITS, ZP, MX, WU, TK>(st, io, b, h, b * st.H + h, has_token, smem + (size_t)warp * L.total, warp);
 }
@@ -1212,7 +1232,9 @@ static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_tok
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)units), dim3(WU * 32), smem, s, attr);
-  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>, d, io, has_token);
+  const int one_wave =
+      units <= (long)device_sm_count() * resident_blocks<decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>>(WU * 32, smem);
+  return cudaLaunchKernelEx(&cfg, decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>, d, io, has_token, one_wave);
 }
 
 // Warps per unit by the size of the pool: while the units fill fewer than a half (a quarter) of the SMs' warp

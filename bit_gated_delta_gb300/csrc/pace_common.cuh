@@ -44,6 +44,20 @@ inline cudaError_t smem_opt_in(size_t bytes) {
   return e;
 }
 
+// Blocks of kernel K (with `threads` threads and `smem` bytes of dynamic shared memory) resident per SM on the current
+// device (queried once per kernel and device).
+template <auto K>
+inline int resident_blocks(int threads, size_t smem) {
+  static std::atomic<int> cache[PACE_MAX_DEVICES];
+  const int dev = current_device();
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, K, threads, smem) != cudaSuccess || v <= 0) v = 1;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 // Sequential carving of a dynamic shared-memory block (16-byte aligned pieces, or `align`).
 __host__ __device__ inline size_t carve(size_t &off, size_t bytes, size_t align = 16) {
   const size_t o = (off + align - 1) & ~(align - 1);
