@@ -32,6 +32,13 @@ namespace pace {
 
 constexpr int DF_TOK = 8;   // buffered tokens the tables hold by default (dP <= 8; 32-token tables: decode_fold_t32.cu)
 
+// Four warps per unit share the token quantization and the Gram products (int4, int8 buffer, 8-token tables).
+template <int WU, int BITS, int MX, int TK>
+__host__ __device__ constexpr bool fold_coop() {
+  return WU == 4 && BITS == 4 && !MX && TK == DF_TOK;
+}
+constexpr size_t FOLD_COOP_BYTES = 2048 + 16;   // 4 warps x 32 lanes x float4 partial Gram, 3 shared scales
+
 struct FoldSmem {
   size_t krow, vrow, ydig, ssc, szp, po, pb, kbf, csx, kf, gram, qk, Lm, tk, ck, total;
 };
@@ -217,6 +224,10 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // the dot loop over M-tiles stays rolled except for the smallest tile body (int4, symmetric, two groups, int8
   // buffer): the larger bodies, fully unrolled, overflow the instruction cache
   constexpr bool DF_ROLL = !(BITS == 4 && NG <= 2 && !ZP && !MX);
+  // four warps per unit (small launches): the warps share the new token's quantization and the Gram products
+  // instead of each staging them, through a shared area after the block's work areas
+  constexpr bool COOP = fold_coop<WU, BITS, MX, TK>();
+  unsigned char *shared_area = wsm + (size_t)(WU - part) * fold_smem(D, G, MX, ZP, BF, TK).total;
   constexpr int OFF = BF ? 0 : 1 << (BITS - 1);
   constexpr int NKG = G / 8;
   static_assert(MTW >= 1 && CPW >= 1, "warps per unit");
@@ -295,6 +306,80 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
 
   // ---- the new token: buffer slot m0 (global and shared), its scalars; q as three int8 digit rows
   float sq = 0.0f;                                 // scale of the q digits
+  if constexpr (COOP) {
+    // warp 0 quantizes k, warp 1 v, warp 2 q: each writes its rows into every warp's work area and its scale into
+    // the shared slots; the buffer entry's scalars follow the barrier
+    float *shs = reinterpret_cast<float *>(shared_area + 2048);
+    if (has_token) {
+      const int col0 = CPL * lane;
+      if (part == 0) {
+        float mk = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) mk = fmaxf(mk, fabsf(tin.kx[c]));
+        const float Ak = warp_max(mk);
+        const bool kz = !(Ak >= FLT_MIN);
+        const float rkk = kz ? 0.0f : __fdiv_rn(127.0f, Ak);
+        const float sk = kz ? 0.0f : __fdiv_rn(Ak, 127.0f);
+        int ck[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) ck[c] = min(max(__float2int_rn(__fmul_rn(tin.kx[c], rkk)), -127), 127);
+#pragma unroll
+        for (int w = 0; w < WU; ++w)
+          dm_store_bytes<CPL>(reinterpret_cast<int8_t *>(wsm + (w - part) * (long)L.total + L.krow) + m0 * RS + col0, ck);
+        if (key_writer(st, unit)) dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_k) + (ku * dP + m0) * D + col0, ck);
+        if (lane == 0) shs[0] = sk;
+      } else if (part == 1) {
+        float mv = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) mv = fmaxf(mv, fabsf(tin.vx[c]));
+        const float Av = warp_max(mv);
+        const bool vz = !(Av >= FLT_MIN);
+        const float rvv = vz ? 0.0f : __fdiv_rn(127.0f, Av);
+        const float sv = vz ? 0.0f : __fdiv_rn(Av, 127.0f);
+        int cv[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) cv[c] = min(max(__float2int_rn(__fmul_rn(tin.vx[c], rvv)), -127), 127);
+#pragma unroll
+        for (int w = 0; w < WU; ++w) dm_store_bytes<CPL>(wsm + (w - part) * (long)L.total + L.vrow + m0 * D + col0, cv);
+        dm_store_bytes<CPL>(static_cast<int8_t *>(st.buf_v) + ((size_t)unit * dP + m0) * D + col0, cv);
+        if (lane == 0) shs[1] = sv;
+      } else if (part == 2) {
+        float mq = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) mq = fmaxf(mq, fabsf(tin.qx[c]));
+        const float Aq = warp_max(mq);
+        const float QMAX = 8323072.0f;
+        const bool qz = !(Aq >= FLT_MIN);
+        const float sqw = qz ? 0.0f : __fdividef(Aq, QMAX);
+        const float rq = qz ? 0.0f : __fdividef(QMAX, Aq);
+        int d2[CPL], d1[CPL], d0[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int qi = min(max(__float2int_rn(tin.qx[c] * rq), -8323072), 8323072);
+          const int q1 = (qi + 128) >> 8;
+          d0[c] = qi - (q1 << 8);
+          d2[c] = (q1 + 128) >> 8;
+          d1[c] = q1 - (d2[c] << 8);
+        }
+#pragma unroll
+        for (int w = 0; w < WU; ++w) {
+          int8_t *kr = reinterpret_cast<int8_t *>(wsm + (w - part) * (long)L.total + L.krow);
+          dm_store_bytes<CPL>(kr + QR * RS + col0, d2);
+          dm_store_bytes<CPL>(kr + (QR + 1) * RS + col0, d1);
+          dm_store_bytes<CPL>(kr + (QR + 2) * RS + col0, d0);
+        }
+        if (lane == 0) shs[2] = sqw;
+      }
+    }
+    __syncthreads();
+    if (has_token) {
+      const float sk = shs[0], sv = shs[1];
+      sq = shs[2];
+      if (lane == m0) bs = make_float4(tin.an, tin.bn, sk, sv);
+      if (part == 0 && lane == 0)
+        *reinterpret_cast<float4 *>(st.buf_s + ((size_t)unit * dP + m0) * 4) = make_float4(tin.an, tin.bn, sk, sv);
+    }
+  } else
   if (has_token) {
     const int col0 = CPL * lane;
     float mk = 0.0f, mv = 0.0f, mq = 0.0f;
@@ -397,7 +482,37 @@ __device__ void df_unit(const PaceDev &st, const PaceIO &io, int b, int h, int u
   // ---- Gram products k_s.k_t and (q digit).k_t: fp16 MMA (the int8 codes and digits are exact in fp16, every sum
   // an exact integer below 2^24), A = [keys 0..7 | q digits] (M), B = keys (N). (An int8 MMA would take the codes as
   // they are, but on this chip it runs at an eighth of the fp16 rate.)
-  if constexpr (TK == DF_TOK) {
+  if constexpr (COOP) {
+    // each warp two of the eight K steps; the partial fragments are summed (exact integers) by every warp
+    float gacc[2][4] = {};
+    const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;
+#pragma unroll
+    for (int j = 0; j < KS / WU; ++j) {
+      const int ks = part * (KS / WU) + j;
+      const int off = 16 * ks + 4 * (tq >> 1);
+      uint32_t a[4];
+      a[0] = i8pair_f16(lds32(krow + g8 * RS + off), sel, false);
+      a[2] = i8pair_f16(lds32(krow + g8 * RS + off + 8), sel, false);
+      a[1] = g8 < 3 ? i8pair_f16(lds32(krow + (QR + g8) * RS + off), sel, false) : 0u;
+      a[3] = g8 < 3 ? i8pair_f16(lds32(krow + (QR + g8) * RS + off + 8), sel, false) : 0u;
+      mma_f16(gacc[j & 1], a, a[0], a[2]);
+    }
+    float4 *gp = reinterpret_cast<float4 *>(shared_area);
+    gp[part * 32 + lane] = make_float4(gacc[0][0] + gacc[1][0], gacc[0][1] + gacc[1][1], gacc[0][2] + gacc[1][2],
+                                       gacc[0][3] + gacc[1][3]);
+    __syncthreads();
+    float4 t = gp[lane];
+#pragma unroll
+    for (int w = 1; w < WU; ++w) {
+      const float4 u = gp[w * 32 + lane];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    *reinterpret_cast<float2 *>(gram + g8 * 8 + 2 * tq) = make_float2(t.x, t.y);
+    if (g8 < 3) *reinterpret_cast<float2 *>(qk + g8 * 8 + 2 * tq) = make_float2(t.z, t.w);
+  } else if constexpr (TK == DF_TOK) {
     float gacc[4][4] = {};   // four independent chains of the K steps
     const uint32_t sel = (tq & 1) ? 0x4342u : 0x4140u;   // the lane's key pair inside its 4-byte load
 #pragma unroll
@@ -1227,7 +1342,7 @@ __global__ void __launch_bounds__(WU * 32, (TK > DF_TOK ? 8 : BITS == 4 ? PACE_D
 template <int D, int G, int BITS, int ZP, int MX, int WU, int TK = DF_TOK>
 static cudaError_t launch_fold_w(const PaceDev &d, const PaceIO &io, int has_token, cudaStream_t s, long units) {
   const FoldSmem L = fold_smem(D, G, MX, ZP, BITS == 16, TK);
-  const size_t smem = (size_t)WU * L.total;
+  const size_t smem = (size_t)WU * L.total + (fold_coop<WU, BITS, MX, TK>() ? FOLD_COOP_BYTES : 0);
   cudaError_t e = smem_opt_in<decode_fold_kernel<D, G, BITS, ZP, MX, WU, TK>>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
