@@ -16,7 +16,7 @@ sample, host cores), `e2e` (the same metric with host buffers: pinned host->devi
 device->host output copy inside the timed region), `bf16_pertoken` (the per-token bf16-state kernel,
 the pages' comparison point), `prefill`, and `clocks`.
 
-`--impl reference` times the CPU oracle (the reference arm of this build) on a bounded sample.
+`--impl reference` times the CPU oracle (the reference arm) on a bounded sample.
 """
 from __future__ import annotations
 

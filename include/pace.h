@@ -36,7 +36,7 @@ extern "C" {
 typedef enum {
   PACE_OK = 0,
   PACE_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or config field */
-  PACE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  PACE_ERR_UNSUPPORTED = 2,  /* valid request this library does not implement */
   PACE_ERR_STATE = 3,        /* state handle cannot take this call (e.g. wrong mode) */
   PACE_ERR_CUDA = 4,         /* a CUDA call failed; see pace_last_error() */
   PACE_ERR_TIMEOUT = 5       /* a bounded device wait gave up (pace_get_status) */
@@ -64,7 +64,7 @@ enum { PACE_IO_BF16 = 0, PACE_IO_F32 = 1 };
 /* Immutable configuration of one state ([P1] 무엇과 다른가, 어떻게 동작하나). */
 typedef struct {
   int n_heads;        /* H, 1..PACE_MAX_HEADS */
-  int d_k, d_v;       /* head dims; this build: d_k == d_v, 64 or 128 */
+  int d_k, d_v;       /* head dims; this library: d_k == d_v, 64 or 128 */
   int max_batch;      /* sequences the device memory is sized for */
   int dP;             /* decode period, 1..PACE_MAX_DP (pages' default 8) */
   int group;          /* key-axis group size g: 32 or 64, divides d_k (PACE-4: 64, PACE-4/8: 32) */
